@@ -1,0 +1,67 @@
+"""Pins the slot / reshape_and_cache / copy_blocks oracle and the KV sizing arithmetic."""
+import numpy as np
+import pytest
+
+from conftest import load_golden
+from oracle import cache_ops
+
+
+def test_slot_formula_example1():
+    # P06 example 1: table [0, 1], bs 4 -> slot(x, 5) = 1 * 4 + 1 = 5; after the
+    # third append the table is [0, 1, 2] and position 8 sits at slot 8
+    assert cache_ops.slot([0, 1], 5, 4) == 5
+    assert [cache_ops.slot([0, 1, 2], p, 4) for p in (6, 7, 8)] == [6, 7, 8]
+    # a scattered table: position 17 of [9, 3] with bs 16 is row 1 of block 3
+    assert cache_ops.slot([9, 3], 17, 16) == 3 * 16 + 1
+
+
+def test_reshape_and_cache_reads_back():
+    rng = np.random.default_rng(0)
+    nb, bs, H, D, T = 6, 16, 2, 8, 5
+    kc = rng.standard_normal((nb, bs, H, D)).astype(np.float16)
+    vc = rng.standard_normal((nb, bs, H, D)).astype(np.float16)
+    k = rng.standard_normal((T, H, D)).astype(np.float16)
+    v = rng.standard_normal((T, H, D)).astype(np.float16)
+    slots = np.array([0, 17, -1, 95, 40], dtype=np.int64)
+    k0, v0 = kc.copy(), vc.copy()
+    cache_ops.reshape_and_cache(k, v, slots, kc, vc)
+    flat_k, flat_v = kc.reshape(nb * bs, H, D), vc.reshape(nb * bs, H, D)
+    touched = set()
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        touched.add(int(s))
+        assert flat_k[s].tobytes() == k[i].tobytes()
+        assert flat_v[s].tobytes() == v[i].tobytes()
+    for s in range(nb * bs):
+        if s not in touched:
+            assert flat_k[s].tobytes() == k0.reshape(nb * bs, H, D)[s].tobytes()
+    with pytest.raises(IndexError):
+        cache_ops.reshape_and_cache(k[:1], v[:1], np.array([nb * bs]), kc, vc)
+
+
+def test_copy_blocks_copies_whole_blocks_only():
+    rng = np.random.default_rng(1)
+    layers = [rng.standard_normal((8, 4, 2, 8)).astype(np.float16) for _ in range(6)]
+    kcs, vcs = layers[:3], layers[3:]
+    before = [c.copy() for c in layers]
+    pairs = np.array([[1, 5], [2, 0]], dtype=np.int64)
+    cache_ops.copy_blocks(kcs, vcs, pairs)
+    for c, c0 in zip(layers, before):
+        assert c[5].tobytes() == c0[1].tobytes()
+        assert c[0].tobytes() == c0[2].tobytes()
+        for b in (1, 2, 3, 4, 6, 7):
+            assert c[b].tobytes() == c0[b].tobytes()
+
+
+def test_kv_sizing_closed_forms():
+    fx = load_golden("kv_sizing.json")
+    from paged_kv_cache_138_gb300 import accounting
+    for c in fx["cases"]:
+        got = accounting.kv_cache_bytes(c["layers"], c["heads"], c["head_dim"], c["tokens"],
+                                        c["bytes_per_elem"])
+        assert got == c["bytes"]
+        if "gib" in c:
+            assert got / 2 ** 30 == c["gib"]
+    # per-step accounting of a decode batch: valid tokens only
+    assert accounting.step_kv_bytes([7, 16, 31, 48, 63], 8, 128) == 165 * 8 * 128 * 2 * 2
