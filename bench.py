@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the paged KV-cache hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one decode step of the workload: (copy_blocks for pending
+copy-on-write pairs,) then per layer reshape_and_cache of the new token and
+paged decode attention over every sequence.  Inputs are synthetic and resident
+in HBM before timing starts.  The default workload is the Llama-2-13B layer
+shape: batch 64, context lengths ~ U[1, 4096], 40 heads MHA, head_dim 128,
+block_size 16 (KV of one step ~2.7 GB, far larger than the 129 MB L2, so no
+flush is needed between steps).
+
+Prints one JSON line.  `value` is KV bytes read per step / device time per step
+(GB/s, whole job over all ranks); `e2e` is the same metric through the same
+public API with the step inputs copied from pinned host memory and the output
+copied back inside the timed region.  `--impl reference` times the CPU fp64
+oracle on the host cores instead (bounded samples of the same workload).
+Under torchrun each rank runs its own copy of the batch (weak scaling, no
+collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-steps/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama2-13b-layer")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_record(kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it still
+    describes the current kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_key)
+        src = os.path.join(ROOT, "paged_kv_cache_138_gb300", "csrc", "paged_attention.cu")
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if rec and rec.get("source_sha256_16") == digest:
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_oracle_sample(step, layer, seqs, heads):
+    """Time the fp64 oracle on a sample of sequences of one layer (host cores).
+    Returns (seconds, KV bytes the sample attends over, threads)."""
+    import numpy as np
+
+    from oracle import attention as oa
+    from oracle import cache_ops as oc
+    from paged_kv_cache_138_gb300 import accounting
+
+    b = step.batch
+    w = b.workload
+    tables = b.block_tables[seqs]
+    lens = b.context_lens[seqs]
+    blocks = sorted({int(x) for row, L in zip(tables, lens) for x in row[:(int(L) + 15) // 16]})
+    remap = {blk: i for i, blk in enumerate(blocks)}
+    import torch
+    idx = torch.tensor(blocks, dtype=torch.long, device=step.k_cache.device)
+    kc = step.k_cache[layer].index_select(0, idx).cpu().numpy()
+    vc = step.v_cache[layer].index_select(0, idx).cpu().numpy()
+    t2 = np.array([[remap.get(int(x), -1) if x >= 0 else -1 for x in row] for row in tables],
+                  dtype=np.int32)
+    slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 for s in b.slot_mapping[seqs]],
+                     dtype=np.int64)
+    q = step.q[layer].cpu().numpy()[seqs]
+    kn = step.k_new[layer].cpu().numpy()[seqs]
+    vn = step.v_new[layer].cpu().numpy()[seqs]
+    si = np.repeat(np.arange(len(seqs), dtype=np.int32), len(heads))
+    hi = np.tile(np.array(heads, dtype=np.int32), len(seqs))
+    t0 = time.perf_counter()
+    oc.reshape_and_cache(kn, vn, slots, kc, vc)
+    oa.paged_attention_decode_rows(q, kc, vc, t2, lens, w.scale, si, hi)
+    dt = time.perf_counter() - t0
+    frac_heads = len(heads) / w.num_q_heads
+    kv = accounting.step_kv_bytes(lens, w.num_kv_heads, w.head_dim) * frac_heads
+    return dt, kv, oa.num_threads()
+
+
+def setup(args, device):
+    from paged_kv_cache_138_gb300 import workloads as wl
+    from paged_kv_cache_138_gb300.engine import DecodeStep
+    from paged_kv_cache_138_gb300.scenario import prepare_batch
+    w = wl.WORKLOADS[args.workload]
+    batch = prepare_batch(w)
+    step = DecodeStep(batch, device=device)
+    return w, batch, step
+
+
+def run_reference(args):
+    """The reference arm: the CPU fp64 oracle, timed on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from oracle.build import build_oracle
+    build_oracle()
+    device = "cuda:0" if torch.cuda.is_available() else "cpu"
+    if device == "cpu":
+        print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to hold the workload"}))
+        return 0
+    from paged_kv_cache_138_gb300 import build as nb
+    nb.build()
+    w, batch, step = setup(args, device)
+    S = batch.num_seqs
+    rng = np.random.default_rng(5)
+    heads = list(range(w.num_q_heads))
+    times, kvs, threads = [], [], 1
+    for i in range(args.warmup + args.steps):
+        seqs = sorted(rng.choice(S, size=min(2, S), replace=False).tolist())
+        dt, kv, threads = cpu_oracle_sample(step, 0, seqs, heads)
+        if i >= args.warmup:
+            times.append(dt)
+            kvs.append(kv)
+    value = sum(kvs) / sum(times) / 1e9
+    sample = "%d steps, each 2 random sequences x all %d heads of 1 layer (fp64 oracle)" % (
+        args.steps, w.num_q_heads)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "description": w.description},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_138_gb300 import accounting
+    from paged_kv_cache_138_gb300 import build as nb
+    if rank == 0:
+        nb.build()
+    if world > 1:
+        torch.distributed.barrier()
+    w, batch, step = setup(args, device)
+    kv_bytes = accounting.step_kv_bytes(batch.context_lens, w.num_kv_heads, w.head_dim,
+                                        layers=w.num_layers)
+    stream = torch.cuda.current_stream(device)
+
+    from paged_kv_cache_138_gb300 import ops
+
+    def one_step():
+        step.apply_cow(stream)
+        step.run(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        one_step()
+    torch.cuda.synchronize(device)
+    step.check_errors()
+
+    # ---- device-resident timed region ----------------------------------------------
+    attn_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps * step.num_layers)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index) as clocks:
+        start.record(stream)
+        k = 0
+        for _ in range(args.steps):
+            step.apply_cow(stream)
+            for i in range(step.num_layers):
+                ops.reshape_and_cache(step.k_new[i], step.v_new[i], step.slot_mapping,
+                                      step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
+                                      stream=stream)
+                attn_events[k][0].record(stream)
+                ops.paged_attention_decode(step.out[i], step.q[i], step.k_cache[i],
+                                           step.v_cache[i], step.block_tables, step.context_lens,
+                                           step.scale, workspace=step.workspace,
+                                           dev_err=step.dev_err, stream=stream)
+                attn_events[k][1].record(stream)
+                k += 1
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    attn_ms = sum(a.elapsed_time(b) for a, b in attn_events) / len(attn_events)
+    step.check_errors()
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * kv_bytes / (ms_per_step / 1e3) / 1e9
+
+    # ---- end to end through the public API from pinned host buffers ----------------
+    e2e_steps = args.e2e_steps or max(3, min(args.steps, 500))
+    h2d, d2h = step.host_bytes_per_step()
+    for _ in range(3):
+        step.apply_cow(stream)
+        step.run_from_host(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        step.apply_cow(stream)
+        step.run_from_host(stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * kv_bytes / (e2e_ms / 1e3) / 1e9
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_kind = hbm_peak()
+    layer_kv = kv_bytes / w.num_layers
+    achieved = layer_kv / (attn_ms / 1e3) / 1e9
+    tr = traffic_record("paged_attention_decode/" + args.workload)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": tr["dram_bytes_per_launch"] if tr else None,
+                "algorithmic_bytes_per_launch": layer_kv,
+                "kernel": "paged_attention_decode (split kernel + LSE merge, CUDA events)",
+                "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import numpy as np
+        rng = np.random.default_rng(3)
+        S = batch.num_seqs
+        order = rng.permutation(S).tolist()
+        tot_t, tot_kv, n_used, threads = 0.0, 0.0, 0, 1
+        while tot_t < 10.0 and n_used < S:
+            seqs = sorted(order[n_used:n_used + 2])
+            dt, kvb, threads = cpu_oracle_sample(step, 0, seqs, list(range(w.num_q_heads)))
+            tot_t += dt
+            tot_kv += kvb
+            n_used += len(seqs)
+        cpu = {"value": tot_kv / tot_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": "%d of %d sequences, all %d heads, layer 0 (fp64 C oracle, %.1f s)" % (
+                   n_used, S, w.num_q_heads, tot_t)}
+    launches = step.kernel_launches_per_step() + (1 if batch.cow_pairs.shape[0] else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "description": w.description,
+                   "num_seqs": batch.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "block_size": w.block_size, "layers": w.num_layers,
+                   "tokens": int(batch.context_lens.sum()), "kv_bytes_per_step": kv_bytes,
+                   "pool_blocks": batch.num_blocks,
+                   "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush"},
+        "seq_steps_per_s": world * batch.num_seqs / (ms_per_step / 1e3),
+        "pct_of_hbm_peak": {"measured": 100 * value / world / peak if peak_kind == "measured"
+                            else None, "nominal_8tbs": 100 * value / world / NOMINAL_HBM_GBS},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,221 @@
+/*
+ * libpagedkv -- paged KV cache hot path for NVIDIA GB300 (sm_103a).
+ *
+ * A C ABI: plain pointers and sizes, no C++ or framework types.  Every function
+ * returns an int status (PKV_OK == 0, negative on error) and never lets a C++
+ * exception out.  Device work is enqueued asynchronously on the caller's stream
+ * (`stream` is a cudaStream_t passed as void*; NULL = the legacy default
+ * stream); nothing here synchronises.  The caller owns every buffer.  All
+ * device pointers must belong to the current CUDA device.
+ *
+ * Metadata that can only be checked on the device (block ids read from a block
+ * table, slots, context lengths) is checked by the kernels.  A bad entry is
+ * skipped -- never trapped -- and the first error code is stored into the
+ * caller's device word `dev_err` (int32, set to 0 by the caller before the
+ * launch; the first error wins through atomicCAS).  Read it after the stream
+ * has been synchronised.
+ *
+ * Terms (after "P06 BlockManager" and "ans20xx day 31"):
+ *   block_size (bs)  tokens per physical KV block; the kernels here take 16
+ *   block table      int32 [num_seqs, max_blocks_per_seq]: logical block i of a
+ *                    sequence is physical block table[s][i]
+ *   slot             physical row of a token: table[pos / bs] * bs + pos % bs
+ *   KV cache         fp16 [num_blocks, block_size, num_kv_heads, head_dim],
+ *                    one tensor for K and one for V per layer
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes (host return values) ---------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)   /* null pointer, negative size, misalignment */
+#define PKV_ERR_UNSUPPORTED (-2)   /* head_dim != 128, block_size != 16, bad GQA ratio */
+#define PKV_ERR_CUDA (-3)          /* a CUDA runtime/driver call failed */
+#define PKV_ERR_OUT_OF_BLOCKS (-4) /* BlockManager: no capacity; state unchanged */
+#define PKV_ERR_BAD_INDEX (-5)     /* unknown sequence, position outside a table */
+
+/* ---- device error codes (stored into *dev_err by the kernels) ------------ */
+#define PKV_DEV_OK 0
+#define PKV_DEV_BAD_BLOCK_ID 1     /* table entry outside [0, num_blocks) */
+#define PKV_DEV_BAD_CONTEXT_LEN 2  /* context_lens[s] < 0 or > max_blocks * bs */
+#define PKV_DEV_BAD_SLOT 3         /* slot >= num_blocks * block_size */
+#define PKV_DEV_WAIT_TIMEOUT 4     /* a bounded wait on a copy gave up */
+#define PKV_DEV_BAD_POSITION 5     /* position outside its block table */
+
+/* Human-readable name of a status code (static string). */
+const char* pkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/* ---- paged decode attention --------------------------------------------- */
+/*
+ * Single-token decode attention over a paged KV cache.
+ * Defined by "qaqbuyan: vLLM PagedAttention" (`paged_attention`: gather each
+ * logical block through the block table, then softmax(q K^T * scale) V) and by
+ * the slot rule of "P06 BlockManager".  For every sequence s and query head h,
+ * with g = h / (num_q_heads / num_kv_heads) and L = context_lens[s]:
+ *   out[s, h, :] = sum_t softmax_t(scale * <q[s, h, :], K_s[t, g, :]>) V_s[t, g, :]
+ * over exactly the L tokens t = 0 .. L-1, where K_s[t] is row t % 16 of
+ * physical block block_tables[s][t / 16].  L == 0 gives a zero row.
+ *
+ *   out        fp16 [num_seqs, num_q_heads, head_dim], written
+ *   q          fp16 [num_seqs, num_q_heads, head_dim]
+ *   k_cache,
+ *   v_cache    fp16 [num_blocks, 16, num_kv_heads, head_dim]; 16-byte aligned
+ *   block_tables int32 [num_seqs, max_blocks_per_seq] (device)
+ *   context_lens int32 [num_seqs] (device); tokens per sequence, the token
+ *              written this step included
+ *   head_dim must be 128, block_size 16, num_q_heads / num_kv_heads in
+ *   {1, 2, 4, 8}; otherwise PKV_ERR_UNSUPPORTED.
+ *   workspace  device scratch of at least
+ *              pkv_paged_attention_workspace_bytes(...) bytes (may be NULL when
+ *              that is 0); holds per-split partial results of long contexts.
+ *              Contents need no initialisation.  Two launches in flight at
+ *              once must not share a workspace.
+ *   dev_err    device int32 (see above); may be NULL to skip reporting.
+ * fp32 accumulation throughout; the result is rounded to fp16 once.
+ */
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                               const void* v_cache, const int32_t* block_tables,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int64_t num_blocks, int max_blocks_per_seq, float scale,
+                               void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                               void* stream);
+
+/* Workspace bytes pkv_paged_attention_decode needs for these sizes (host only). */
+size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
+                                           int max_blocks_per_seq, int head_dim);
+
+/* ---- cache write --------------------------------------------------------- */
+/*
+ * reshape_and_cache: store the K/V of new tokens at their slots.
+ * "ans20xx day 31": a decoded token is written into the last, not yet full block
+ * of its sequence; "P06 BlockManager" gives its slot.  For i < num_tokens:
+ *   k_cache[slot / bs, slot % bs, :, :] = k[i, :, :]   (same for v)
+ * with slot = slot_mapping[i].  A negative slot skips the token (padding); a slot
+ * >= num_blocks * block_size is skipped and reported as PKV_DEV_BAD_SLOT.
+ * Two tokens with the same slot in one call race (undefined which lands).
+ *   k, v        fp16 [num_tokens, num_kv_heads, head_dim], 16-byte aligned
+ *   slot_mapping int64 [num_tokens] (device)
+ *   k_cache, v_cache fp16 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   num_kv_heads * head_dim must be a multiple of 8.  Bit-exact copy.
+ */
+int pkv_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache, int num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int64_t num_blocks, int32_t* dev_err,
+                          void* stream);
+
+/*
+ * Slot mapping on the device: slot_mapping[s] = table[s][p / bs] * bs + p % bs
+ * with p = positions[s] ("P06 BlockManager", problem summary).  p < 0 gives -1
+ * (no write).  p >= max_blocks_per_seq * bs or a table entry outside
+ * [0, num_blocks) gives -1 and PKV_DEV_BAD_POSITION / PKV_DEV_BAD_BLOCK_ID.
+ *   block_tables int32 [num_seqs, max_blocks_per_seq], positions int32
+ *   [num_seqs], slot_mapping int64 [num_seqs]; all device.
+ */
+int pkv_slot_mapping(const int32_t* block_tables, const int32_t* positions, int num_seqs,
+                     int max_blocks_per_seq, int block_size, int64_t num_blocks,
+                     int64_t* slot_mapping, int32_t* dev_err, void* stream);
+
+/* ---- copy-on-write block copy -------------------------------------------- */
+/*
+ * copy_blocks: for every pair (src, dst) and every layer,
+ *   k_caches[layer][dst] = k_caches[layer][src]   (same for v_caches)
+ * copying the whole block.  "ans20xx day 31", toy COW append: when a sequence
+ * writes into a block it still shares after a fork, it takes a new block and
+ * the old block's KV is copied into it (the page copies the valid bytes; the
+ * whole block is copied here, so dst equals src byte for byte).
+ *   k_caches, v_caches  HOST arrays of num_layers device pointers (1..64 layers)
+ *   block_pairs  int64 [num_pairs, 2] (device), (src, dst) per row; ids outside
+ *                [0, num_blocks) are skipped and reported as PKV_DEV_BAD_BLOCK_ID
+ *   block_bytes  bytes of one block of one cache (16 * num_kv_heads * head_dim * 2
+ *                for fp16); a multiple of 16, pointers 16-byte aligned
+ * A dst that is also another pair's src, or two pairs with one dst, race.
+ */
+int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                    const int64_t* block_pairs, int num_pairs, int64_t block_bytes,
+                    int64_t num_blocks, int32_t* dev_err, void* stream);
+
+/* ---- host BlockManager ---------------------------------------------------- */
+/*
+ * The BlockManager of "P06 BlockManager" (free list taken FIFO, reference
+ * counts, chained block hashes with at most (len - 1) / bs matchable blocks, an
+ * LRU pool of evictable cached blocks, atomic allocate/append, reverse-order
+ * free), plus fork and copy-on-write from "ans20xx day 31".  Host memory only,
+ * single-threaded: one handle must not be used from two threads at once.
+ * Sequence ids are caller-chosen int64 values.  Operations that fail with
+ * PKV_ERR_OUT_OF_BLOCKS leave every piece of state unchanged.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* initial_free_order: NULL for 0..num_blocks-1, or a permutation of it (the
+ * order in which free blocks are handed out).  Returns NULL on bad arguments. */
+pkv_block_manager* pkv_bm_create(int64_t num_blocks, int block_size, int enable_prefix_cache,
+                                 const int32_t* initial_free_order);
+void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Allocate a new sequence holding num_tokens prompt tokens.  Writes its block
+ * table (up to table_cap entries) and sets *num_table_blocks and
+ * *num_cached_tokens (prefix-cache hits x bs).  PKV_ERR_INVALID_ARG if the id
+ * is in use or table_cap is too small (state unchanged). */
+int pkv_bm_allocate(pkv_block_manager* bm, int64_t seq_id, const int32_t* tokens,
+                    int64_t num_tokens, int32_t* table_out, int64_t table_cap,
+                    int64_t* num_table_blocks, int64_t* num_cached_tokens);
+
+/* Append one token; *slot_out receives its slot.  Takes a new block at a block
+ * boundary, or -- when the partial last block is shared after a fork -- a
+ * private copy whose (old, new) pair is queued for pkv_bm_take_cow_pairs. */
+int pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int32_t token, int64_t* slot_out);
+
+/* Append one token to each of n sequences, in order; slots_out[i] receives each
+ * slot.  Stops at the first failure and returns its status with
+ * *num_done = appends completed (each completed append stays). */
+int pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, const int32_t* tokens,
+                        int64_t n, int64_t* slots_out, int64_t* num_done);
+
+/* child shares every block of parent (ref + 1 each) and copies its tokens. */
+int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
+
+/* Release a sequence (unknown ids are ignored; never fails). */
+int pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
+
+int pkv_bm_slot(const pkv_block_manager* bm, int64_t seq_id, int64_t pos, int64_t* slot_out);
+int64_t pkv_bm_num_free_blocks(const pkv_block_manager* bm);
+/* The coarse check ceil(num_tokens / bs) <= num_free_blocks: 1 or 0. */
+int pkv_bm_can_allocate(const pkv_block_manager* bm, int64_t num_tokens);
+/* Table length of a sequence (or PKV_ERR_BAD_INDEX); copies up to cap entries. */
+int64_t pkv_bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out, int64_t cap);
+int64_t pkv_bm_num_tokens(const pkv_block_manager* bm, int64_t seq_id);
+int64_t pkv_bm_num_cached_tokens(const pkv_block_manager* bm, int64_t seq_id);
+/* Rows [n, max_blocks] of block tables (pad entries past each table) and the
+ * token counts of the listed sequences, ready for the attention kernel. */
+int pkv_bm_fill_block_tables(const pkv_block_manager* bm, const int64_t* seq_ids, int64_t n,
+                             int32_t* tables_out, int64_t max_blocks, int32_t pad,
+                             int32_t* context_lens_out);
+/* Pending copy-on-write pairs: returns their count; when cap_pairs is at least
+ * that count the pairs are written to out ([count, 2] int64) and drained. */
+int64_t pkv_bm_take_cow_pairs(pkv_block_manager* bm, int64_t* out, int64_t cap_pairs);
+
+/* Introspection (tests): free list in hand-out order, evictable pool oldest
+ * first, reference counts [num_blocks].  Return the element count. */
+int64_t pkv_bm_free_list(const pkv_block_manager* bm, int32_t* out, int64_t cap);
+int64_t pkv_bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int64_t cap);
+int64_t pkv_bm_ref_counts(const pkv_block_manager* bm, int32_t* out, int64_t cap);
+/* 0 when invariants I1..I5 of "P06 BlockManager" hold, else the number of the
+ * first one violated (1..5). */
+int pkv_bm_check_invariants(const pkv_block_manager* bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

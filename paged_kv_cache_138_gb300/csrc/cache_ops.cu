@@ -1,0 +1,167 @@
+// Cache-consistency kernels for sm_103a: reshape_and_cache (scatter of new
+// K/V rows to their slots), the device slot mapping and copy_blocks (the
+// copy-on-write block copy).  All are bit-exact data movement with 16-byte
+// vector accesses; each checks the indices it reads and skips a bad one after
+// recording it in dev_err.
+#include <algorithm>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace cache {
+
+constexpr int kThreads = 256;
+
+// One thread moves one 16-byte vector of K and the matching vector of V.
+// The cache [num_blocks, bs, Hkv, D] viewed as rows of Hkv*D halves has the
+// token of slot `slot` at row `slot` (block slot/bs, offset slot%bs).
+__global__ void __launch_bounds__(kThreads)
+    reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             const int64_t* __restrict__ slots, uint4* __restrict__ kc,
+                             uint4* __restrict__ vc, int64_t total, int row_vecs,
+                             int64_t num_slots, int32_t* dev_err) {
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+  if (idx >= total) return;
+  const int64_t i = idx / row_vecs;
+  const int c = static_cast<int>(idx - i * row_vecs);
+  const int64_t slot = __ldg(slots + i);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (c == 0) report(dev_err, PKV_DEV_BAD_SLOT);
+    return;
+  }
+  const uint4 kv = __ldg(k + i * row_vecs + c);
+  const uint4 vv = __ldg(v + i * row_vecs + c);
+  kc[slot * row_vecs + c] = kv;
+  vc[slot * row_vecs + c] = vv;
+}
+
+__global__ void __launch_bounds__(kThreads)
+    slot_mapping_kernel(const int32_t* __restrict__ tables, const int32_t* __restrict__ positions,
+                        int num_seqs, int max_blocks, int block_size, int64_t num_blocks,
+                        int64_t* __restrict__ slots, int32_t* dev_err) {
+  const int s = blockIdx.x * kThreads + threadIdx.x;
+  if (s >= num_seqs) return;
+  const int32_t pos = __ldg(positions + s);
+  int64_t slot = -1;
+  if (pos >= 0) {
+    const int32_t logical = pos / block_size;
+    if (logical >= max_blocks) {
+      report(dev_err, PKV_DEV_BAD_POSITION);
+    } else {
+      const int32_t b = __ldg(tables + static_cast<int64_t>(s) * max_blocks + logical);
+      if (b < 0 || b >= num_blocks)
+        report(dev_err, PKV_DEV_BAD_BLOCK_ID);
+      else
+        slot = static_cast<int64_t>(b) * block_size + pos % block_size;
+    }
+  }
+  slots[s] = slot;
+}
+
+constexpr int kMaxLayersPerLaunch = 64;
+struct LayerPtrs {
+  uint4* k[kMaxLayersPerLaunch];
+  uint4* v[kMaxLayersPerLaunch];
+};
+
+// grid (pairs, layers, 2 caches): one CTA copies one block of one cache.
+__global__ void __launch_bounds__(kThreads)
+    copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs, const int64_t* __restrict__ pairs,
+                       int64_t block_vecs, int64_t num_blocks, int32_t* dev_err) {
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int64_t src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && layer == 0 && blockIdx.z == 0) report(dev_err, PKV_DEV_BAD_BLOCK_ID);
+    return;
+  }
+  if (src == dst) return;
+  uint4* base = blockIdx.z ? ptrs.v[layer] : ptrs.k[layer];
+  const uint4* __restrict__ from = base + src * block_vecs;
+  uint4* __restrict__ to = base + dst * block_vecs;
+  constexpr int kUnroll = 4;
+  int64_t i = threadIdx.x;
+  for (; i + (kUnroll - 1) * kThreads < block_vecs; i += kUnroll * kThreads) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) r[u] = __ldg(from + i + u * kThreads);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) to[i + u * kThreads] = r[u];
+  }
+  for (; i < block_vecs; i += kThreads) to[i] = __ldg(from + i);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace cache
+}  // namespace pkv
+
+extern "C" int pkv_reshape_and_cache(const void* k, const void* v, const int64_t* slot_mapping,
+                                     void* k_cache, void* v_cache, int num_tokens,
+                                     int num_kv_heads, int head_dim, int block_size,
+                                     int64_t num_blocks, int32_t* dev_err, void* stream) {
+  using namespace pkv::cache;
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if ((static_cast<int64_t>(num_kv_heads) * head_dim) % 8 != 0) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  const int64_t row_vecs64 = static_cast<int64_t>(num_kv_heads) * head_dim / 8;
+  if (row_vecs64 > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int row_vecs = static_cast<int>(row_vecs64);
+  const int64_t total = static_cast<int64_t>(num_tokens) * row_vecs;
+  const int64_t blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), kThreads, 0,
+                             static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), total, row_vecs,
+      num_blocks * block_size, dev_err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_slot_mapping(const int32_t* block_tables, const int32_t* positions,
+                                int num_seqs, int max_blocks_per_seq, int block_size,
+                                int64_t num_blocks, int64_t* slot_mapping, int32_t* dev_err,
+                                void* stream) {
+  using namespace pkv::cache;
+  if (num_seqs < 0 || max_blocks_per_seq <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!block_tables || !positions || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  slot_mapping_kernel<<<(num_seqs + kThreads - 1) / kThreads, kThreads, 0,
+                        static_cast<cudaStream_t>(stream)>>>(
+      block_tables, positions, num_seqs, max_blocks_per_seq, block_size, num_blocks, slot_mapping,
+      dev_err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                               const int64_t* block_pairs, int num_pairs, int64_t block_bytes,
+                               int64_t num_blocks, int32_t* dev_err, void* stream) {
+  using namespace pkv::cache;
+  if (num_layers < 0 || num_pairs < 0 || block_bytes <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (block_bytes % 16 != 0) return PKV_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PKV_OK;
+  if (!k_caches || !v_caches || !block_pairs) return PKV_ERR_INVALID_ARG;
+  if (num_pairs > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  for (int base = 0; base < num_layers; base += kMaxLayersPerLaunch) {
+    const int n = std::min(kMaxLayersPerLaunch, num_layers - base);
+    LayerPtrs ptrs;
+    for (int i = 0; i < kMaxLayersPerLaunch; ++i) ptrs.k[i] = ptrs.v[i] = nullptr;
+    for (int i = 0; i < n; ++i) {
+      void* kp = k_caches[base + i];
+      void* vp = v_caches[base + i];
+      if (!kp || !vp || !aligned16(kp) || !aligned16(vp)) return PKV_ERR_INVALID_ARG;
+      ptrs.k[i] = static_cast<uint4*>(kp);
+      ptrs.v[i] = static_cast<uint4*>(vp);
+    }
+    copy_blocks_kernel<<<dim3(num_pairs, n, 2), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        ptrs, block_pairs, block_bytes / 16, num_blocks, dev_err);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}

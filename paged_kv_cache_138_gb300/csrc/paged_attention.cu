@@ -1,0 +1,473 @@
+// Paged decode attention for sm_103a.
+//
+// What it computes ("qaqbuyan: vLLM PagedAttention", `paged_attention`; slot
+// rule of "P06 BlockManager"): for every sequence s and query head h,
+//   out[s,h] = softmax(scale * q[s,h] . K_s^T) V_s
+// over the L = context_lens[s] tokens whose K/V rows sit in physical blocks
+// block_tables[s][t / 16], row t % 16.
+//
+// How (GB300 design, not the pages' sketch):
+//  * One CTA per (KV head g, sequence s, split of up to 32 physical blocks).
+//    The G = Hq / Hkv query heads that read KV head g are handled together, so
+//    every K/V byte is read from HBM once per step.
+//  * Each of the 4 warps streams its own blocks of the split (warp w takes
+//    blocks w, w+4, ...) through a private 3-stage ring in shared memory.  A
+//    stage is one physical block of one KV head: four TMA tiles of 16 rows x
+//    64 dims (K lo/hi, V lo/hi), 8 KB, 128-byte swizzled, completion counted on
+//    one mbarrier.  Lane 0 refills a stage as soon as the warp is done with it.
+//  * QK: lane (t, half) = (lane % 16, lane / 16) dots token t with 64 dims of
+//    each of the G queries (q pre-scaled by scale*log2 e, fp32 in smem); one
+//    shuffle joins the halves.  Packed fp32x2 FMAs.
+//  * Online softmax in base 2 per warp, with a lazy rescale: the running max
+//    only moves when a block max exceeds it by more than 8, so most blocks do
+//    no rescaling and every weight stays <= 2^8.
+//  * PV: lane owns 4 of the 128 output dims for each query, weights broadcast
+//    from smem; tokens past L are never multiplied (no 0 * garbage).
+//  * The 4 warps' (m, l, o) are merged in smem.  Sequences that need one split
+//    write fp16 output directly; longer ones write fp32 partials that a second
+//    small kernel merges by log-sum-exp.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+namespace attn {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockSize = 16;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kStages = 3;
+constexpr int kPartitionBlocks = 32;                    // physical blocks per CTA
+constexpr int kHalfTileBytes = kBlockSize * 64 * 2;     // 16 rows x 128 B
+constexpr int kStageBytes = 4 * kHalfTileBytes;         // K lo, K hi, V lo, V hi
+constexpr float kRescaleThreshold = 8.0f;               // log2 units
+
+template <int G>
+struct Smem {
+  static constexpr int stages = 0;
+  static constexpr int stages_bytes = kWarps * kStages * kStageBytes;
+  static constexpr int q = stages + stages_bytes;                    // float [G][128]
+  static constexpr int p = q + G * kHeadDim * 4;                     // float [warps][16][G]
+  static constexpr int bars = p + kWarps * kBlockSize * G * 4;       // u64 [warps][stages]
+  static constexpr int table = bars + kWarps * kStages * 8;          // int32 [partition]
+  static constexpr int ml = table + kPartitionBlocks * 4;            // float [warps][G][2]
+  static constexpr int total = ml + kWarps * G * 2 * 4;
+  static constexpr int alloc = total + 1024;                         // alignment slack
+  static_assert(kWarps * G * kHeadDim * 4 <= stages_bytes, "merge buffer must fit");
+};
+
+struct Params {
+  __half* out;
+  const __half* q;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float* part_o;   // [S, Hq, max_splits, 128]
+  float* part_ml;  // [S, Hq, max_splits, 2]  (max, sum) in log2 units
+  int32_t* dev_err;
+  int64_t num_blocks;
+  int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits;
+  float scale_log2;
+};
+
+__device__ __forceinline__ int clamp_context(const Params& p, int s, bool may_report) {
+  int L = __ldg(p.context_lens + s);
+  const int cap = p.max_blocks * kBlockSize;
+  if (L < 0 || L > cap) {
+    if (may_report) report(p.dev_err, PKV_DEV_BAD_CONTEXT_LEN);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+template <int G>
+__device__ __forceinline__ void process_block(const uint8_t* st, const float* q_s, float* p_s,
+                                              int valid, int lane, float (&m)[G], float (&l)[G],
+                                              float2 (&o)[G][2]) {
+  constexpr unsigned kFull = 0xffffffffu;
+  const int t = lane & 15, half = lane >> 4;
+  // ---- scores: token t, dims [64*half, 64*half + 64) -----------------------
+  const uint8_t* krow = st + half * kHalfTileBytes + t * 128;
+  const int sw = t & 7;
+  float2 acc[G];
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) acc[gi] = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(krow + ((j ^ sw) << 4));
+    const float2 k0 = half2_to_float2(raw.x), k1 = half2_to_float2(raw.y);
+    const float2 k2 = half2_to_float2(raw.z), k3 = half2_to_float2(raw.w);
+#pragma unroll
+    for (int gi = 0; gi < G; ++gi) {
+      const float4 qa = *reinterpret_cast<const float4*>(q_s + gi * kHeadDim + half * 64 + j * 8);
+      const float4 qb =
+          *reinterpret_cast<const float4*>(q_s + gi * kHeadDim + half * 64 + j * 8 + 4);
+      acc[gi] = ffma2(k0, make_float2(qa.x, qa.y), acc[gi]);
+      acc[gi] = ffma2(k1, make_float2(qa.z, qa.w), acc[gi]);
+      acc[gi] = ffma2(k2, make_float2(qb.x, qb.y), acc[gi]);
+      acc[gi] = ffma2(k3, make_float2(qb.z, qb.w), acc[gi]);
+    }
+  }
+  // ---- online softmax (base 2) -----------------------------------------------
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) {
+    float sc = acc[gi].x + acc[gi].y;
+    sc += __shfl_xor_sync(kFull, sc, 16);
+    sc = t < valid ? sc : -INFINITY;
+    float bm = sc;
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
+    if (bm > m[gi] + kRescaleThreshold) {  // warp-uniform
+      const float alpha = exp2_approx(m[gi] - bm);
+      const float2 a2 = make_float2(alpha, alpha);
+      l[gi] *= alpha;
+      o[gi][0] = fmul2(o[gi][0], a2);
+      o[gi][1] = fmul2(o[gi][1], a2);
+      m[gi] = bm;
+    }
+    const float w = exp2_approx(sc - m[gi]);
+    float ws = w;
+    ws += __shfl_xor_sync(kFull, ws, 1);
+    ws += __shfl_xor_sync(kFull, ws, 2);
+    ws += __shfl_xor_sync(kFull, ws, 4);
+    ws += __shfl_xor_sync(kFull, ws, 8);
+    l[gi] += ws;
+    if (half == 0) p_s[t * G + gi] = w;
+  }
+  __syncwarp();
+  // ---- weighted values: lane owns dims [4*lane, 4*lane + 4) ------------------
+  const int hv = lane >> 4;
+  const int chunk = (lane & 15) >> 1;
+  const uint8_t* vbase = st + (2 + hv) * kHalfTileBytes + (lane & 1) * 8;
+#pragma unroll
+  for (int tt = 0; tt < kBlockSize; ++tt) {
+    if (tt < valid) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(vbase + tt * 128 + ((chunk ^ (tt & 7)) << 4));
+      const float2 v01 = half2_to_float2(raw.x), v23 = half2_to_float2(raw.y);
+      float w[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int gi = 0; gi < G; gi += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(p_s + tt * G + gi);
+          w[gi] = w4.x; w[gi + 1] = w4.y; w[gi + 2] = w4.z; w[gi + 3] = w4.w;
+        }
+      } else if constexpr (G == 2) {
+        const float2 w2 = *reinterpret_cast<const float2*>(p_s + tt * G);
+        w[0] = w2.x; w[1] = w2.y;
+      } else {
+#pragma unroll
+        for (int gi = 0; gi < G; ++gi) w[gi] = p_s[tt * G + gi];
+      }
+#pragma unroll
+      for (int gi = 0; gi < G; ++gi) {
+        const float2 w2 = make_float2(w[gi], w[gi]);
+        o[gi][0] = ffma2(v01, w2, o[gi][0]);
+        o[gi][1] = ffma2(v23, w2, o[gi][1]);
+      }
+    }
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                 const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  using SM = Smem<G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+
+  const int g = blockIdx.x, s = blockIdx.y, split = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads;
+  const int h0 = g * G;
+
+  const int L = clamp_context(p, s, threadIdx.x == 0 && g == 0 && split == 0);
+  const int nblk = (L + kBlockSize - 1) / kBlockSize;
+  const int nsplit = (nblk + kPartitionBlocks - 1) / kPartitionBlocks;
+  if (L == 0) {
+    if (split == 0) {
+      __half* o = p.out + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
+      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) o[i] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  const int blk_begin = split * kPartitionBlocks;
+  if (blk_begin >= nblk) return;
+  const int n_here = min(kPartitionBlocks, nblk - blk_begin);
+
+  int32_t* tab = reinterpret_cast<int32_t*>(smem + SM::table);
+  float* q_s = reinterpret_cast<float*>(smem + SM::q);
+  float* p_s = reinterpret_cast<float*>(smem + SM::p) + warp * kBlockSize * G;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bars) + warp * kStages;
+  uint8_t* ring = smem + SM::stages + warp * kStages * kStageBytes;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_k);
+    prefetch_tmap(&tmap_v);
+  }
+  const int32_t* trow = p.block_tables + static_cast<int64_t>(s) * p.max_blocks + blk_begin;
+  for (int i = threadIdx.x; i < n_here; i += kThreads) {
+    int32_t b = __ldg(trow + i);
+    if (b < 0 || b >= p.num_blocks) {
+      report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
+      b = -1;
+    }
+    tab[i] = b;
+  }
+  const __half* qp = p.q + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
+  for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads)
+    q_s[i] = __half2float(qp[i]) * p.scale_log2;
+  if (lane == 0) {
+    for (int j = 0; j < kStages; ++j) mbar_init(&bars[j], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
+  auto issue = [&](int k) {  // lane 0 only: load local block k of this warp
+    const int32_t b = tab[warp + k * kWarps];
+    uint64_t* bar = &bars[k % kStages];
+    uint8_t* st = ring + (k % kStages) * kStageBytes;
+    if (b < 0) {  // reported already: complete the phase without data
+      mbar_arrive(bar);
+      return;
+    }
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    const int row = b * kBlockSize;
+    tma_load_3d(st, &tmap_k, 0, g, row, bar);
+    tma_load_3d(st + kHalfTileBytes, &tmap_k, 64, g, row, bar);
+    tma_load_3d(st + 2 * kHalfTileBytes, &tmap_v, 0, g, row, bar);
+    tma_load_3d(st + 3 * kHalfTileBytes, &tmap_v, 64, g, row, bar);
+  };
+
+  int issued = min(kStages, my_count);
+  if (lane == 0)
+    for (int k = 0; k < issued; ++k) issue(k);
+
+  float m[G], l[G];
+  float2 o[G][2];
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) {
+    m[gi] = -INFINITY;
+    l[gi] = 0.f;
+    o[gi][0] = o[gi][1] = make_float2(0.f, 0.f);
+  }
+  bool ok = true;
+  for (int k = 0; k < issued; ++k) {
+    const int stage = k % kStages;
+    const bool landed = mbar_wait_bounded(&bars[stage], (k / kStages) & 1, p.dev_err);
+    ok = __all_sync(0xffffffffu, ok && landed) != 0;
+    const int li = warp + k * kWarps;
+    if (ok && tab[li] >= 0) {
+      const int valid = min(kBlockSize, L - (blk_begin + li) * kBlockSize);
+      process_block<G>(ring + stage * kStageBytes, q_s, p_s, valid, lane, m, l, o);
+    }
+    __syncwarp();
+    if (ok && issued < my_count) {
+      if (lane == 0) issue(issued);
+      ++issued;
+    }
+  }
+
+  // ---- merge the 4 warps' partial softmax states ------------------------------
+  __syncthreads();  // every issued tile has landed (or timed out); ring is free
+  float* ml = reinterpret_cast<float*>(smem + SM::ml);
+  float* ob = reinterpret_cast<float*>(smem + SM::stages);
+#pragma unroll
+  for (int gi = 0; gi < G; ++gi) {
+    if (lane == 0) {
+      ml[(warp * G + gi) * 2] = m[gi];
+      ml[(warp * G + gi) * 2 + 1] = l[gi];
+    }
+    *reinterpret_cast<float4*>(ob + (warp * G + gi) * kHeadDim + lane * 4) =
+        make_float4(o[gi][0].x, o[gi][0].y, o[gi][1].x, o[gi][1].y);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
+    const int gi = e / kHeadDim, d = e % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * G + gi) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float c = exp2_approx(ml[(w * G + gi) * 2] - M);
+        num += c * ob[(w * G + gi) * kHeadDim + d];
+        den += c * ml[(w * G + gi) * 2 + 1];
+      }
+    }
+    const int64_t row = static_cast<int64_t>(s) * Hq + h0 + gi;
+    if (nsplit == 1) {
+      p.out[row * kHeadDim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    } else {
+      const int64_t slot = row * p.max_splits + split;
+      p.part_o[slot * kHeadDim + d] = num;
+      if (d == 0) {
+        p.part_ml[slot * 2] = M;
+        p.part_ml[slot * 2 + 1] = den;
+      }
+    }
+  }
+}
+
+// Log-sum-exp merge of the splits of one (sequence, query head); 128 threads,
+// one output dim each.  Rows that needed a single split were written directly.
+__global__ void __launch_bounds__(kHeadDim)
+    paged_attention_merge_kernel(const Params p) {
+  const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+  const int L = clamp_context(p, s, false);
+  const int nblk = (L + kBlockSize - 1) / kBlockSize;
+  const int nsplit = (nblk + kPartitionBlocks - 1) / kPartitionBlocks;
+  if (nsplit <= 1) return;
+  const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + h;
+  const float* ml = p.part_ml + row * p.max_splits * 2;
+  const float* po = p.part_o + row * p.max_splits * kHeadDim;
+  float M = -INFINITY;
+  for (int i = 0; i < nsplit; ++i) M = fmaxf(M, ml[2 * i]);
+  float num = 0.f, den = 0.f;
+  if (M != -INFINITY) {
+    for (int i = 0; i < nsplit; ++i) {
+      const float c = exp2_approx(ml[2 * i] - M);
+      num += c * po[i * kHeadDim + d];
+      den += c * ml[2 * i + 1];
+    }
+  }
+  p.out[row * kHeadDim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+}
+
+// ---- host side ------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// The cache [num_blocks * 16 rows, Hkv, 128] as a 3-D tensor; a box is 16 rows
+// x 1 head x 64 dims (128 B inner extent, 128-byte swizzle).
+bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int64_t num_blocks) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_kv_heads),
+                        static_cast<cuuint64_t>(num_blocks) * kBlockSize};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                           static_cast<cuuint64_t>(num_kv_heads) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockSize)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int max_splits_for(int max_blocks) { return (max_blocks + kPartitionBlocks - 1) / kPartitionBlocks; }
+
+template <int G>
+int launch(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, cudaStream_t stream) {
+  // The shared-memory opt-in is per device; remember it for up to 64 devices.
+  static std::atomic<uint8_t> opted_in[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(paged_attention_split_kernel<G>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<G>::alloc) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    if (dev >= 0 && dev < 64) opted_in[dev].store(1, std::memory_order_release);
+  }
+  dim3 grid(p.num_kv_heads, p.num_seqs, p.max_splits);
+  paged_attention_split_kernel<G><<<grid, kThreads, Smem<G>::alloc, stream>>>(mk, mv, p);
+  if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  if (p.max_splits > 1) {
+    paged_attention_merge_kernel<<<dim3(p.num_q_heads, p.num_seqs), kHeadDim, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+extern "C" size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
+                                                      int max_blocks_per_seq, int head_dim) {
+  using namespace pkv::attn;
+  if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || head_dim != kHeadDim)
+    return 0;
+  const int splits = max_splits_for(max_blocks_per_seq);
+  if (splits <= 1) return 0;
+  return static_cast<size_t>(num_seqs) * num_q_heads * splits * (kHeadDim + 2) * sizeof(float);
+}
+
+extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          const int32_t* context_lens, int num_seqs,
+                                          int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int64_t num_blocks,
+                                          int max_blocks_per_seq, float scale, void* workspace,
+                                          size_t workspace_bytes, int32_t* dev_err,
+                                          void* stream) {
+  using namespace pkv::attn;
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (head_dim != kHeadDim || block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return PKV_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return PKV_ERR_INVALID_ARG;
+  if (num_blocks > INT32_MAX / kBlockSize || num_seqs > 65535 || num_kv_heads > 65535)
+    return PKV_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * kBlockSize > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const size_t need = pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
+                                                          max_blocks_per_seq, head_dim);
+  if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15) return PKV_ERR_INVALID_ARG;
+
+  Params p;
+  p.out = static_cast<__half*>(out);
+  p.q = static_cast<const __half*>(q);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.max_splits = max_splits_for(max_blocks_per_seq);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_ml = need ? p.part_o + static_cast<size_t>(num_seqs) * num_q_heads * p.max_splits *
+                                    kHeadDim
+                   : nullptr;
+  p.dev_err = dev_err;
+  p.num_blocks = num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_blocks = max_blocks_per_seq;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  CUtensorMap mk, mv;
+  if (!make_cache_map(&mk, k_cache, num_kv_heads, num_blocks) ||
+      !make_cache_map(&mv, v_cache, num_kv_heads, num_blocks))
+    return PKV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (G) {
+    case 1: return launch<1>(mk, mv, p, st);
+    case 2: return launch<2>(mk, mv, p, st);
+    case 4: return launch<4>(mk, mv, p, st);
+    default: return launch<8>(mk, mv, p, st);
+  }
+}

@@ -1,0 +1,113 @@
+"""Device state and the decode step: per layer, reshape_and_cache then attention.
+
+``DecodeStep`` owns the KV cache of every layer ([layers, num_blocks, 16, Hkv,
+128] fp16 for K and for V), the step's inputs (q, the new token's k/v, slot
+mapping, block tables, context lengths), the output and the attention
+workspace, all resident in HBM.  ``run()`` enqueues one decode step through
+the C ABI; ``run_from_host()`` is the same step fed from pinned host buffers,
+with the host->device copies of the inputs and the device->host copy of the
+output inside it.
+"""
+import numpy as np
+import torch
+
+from . import ops
+from . import workloads as wl
+from .scenario import DecodeBatch
+
+
+class DecodeStep:
+    def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None):
+        """host_values: None draws q/K/V on the device (torch generator seeded by
+        the workload); otherwise the tuple of ``workloads.host_tensors`` (numpy)."""
+        w = batch.workload
+        self.batch = batch
+        self.device = torch.device(device or "cuda")
+        L = num_layers or w.num_layers
+        S, Hq, Hkv, D, bs = batch.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+        self.num_layers, self.scale = L, w.scale
+        dev = self.device
+        if host_values is None:
+            self.k_cache = torch.empty((L, batch.num_blocks, bs, Hkv, D), dtype=torch.float16,
+                                       device=dev)
+            self.v_cache = torch.empty_like(self.k_cache)
+            self.q = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
+            self.k_new = torch.empty((L, S, Hkv, D), dtype=torch.float16, device=dev)
+            self.v_new = torch.empty_like(self.k_new)
+            for i, t in enumerate((self.k_cache, self.v_cache, self.q, self.k_new, self.v_new)):
+                wl.device_normal_fp16_(t, w.seed * 16 + i)
+        else:
+            q, k_new, v_new, k_cache, v_cache = host_values
+            self.q = torch.from_numpy(q).to(dev)
+            self.k_new = torch.from_numpy(k_new).to(dev)
+            self.v_new = torch.from_numpy(v_new).to(dev)
+            self.k_cache = torch.from_numpy(k_cache).to(dev)
+            self.v_cache = torch.from_numpy(v_cache).to(dev)
+        self.block_tables = torch.from_numpy(batch.block_tables).to(dev)
+        self.context_lens = torch.from_numpy(batch.context_lens).to(dev)
+        self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(dev)
+        self.cow_pairs = torch.from_numpy(batch.cow_pairs).to(dev)
+        self.out = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
+        self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev)
+        self.dev_err = ops.new_error_word(dev)
+        self._host = None
+
+    # ---- device-resident step ---------------------------------------------------
+    def apply_cow(self, stream=None):
+        """copy_blocks for the batch's copy-on-write pairs, every layer."""
+        if self.cow_pairs.shape[0] == 0:
+            return
+        ops.copy_blocks([self.k_cache[i] for i in range(self.num_layers)],
+                        [self.v_cache[i] for i in range(self.num_layers)],
+                        self.cow_pairs, dev_err=self.dev_err, stream=stream)
+
+    def run_layer(self, i, stream=None):
+        ops.reshape_and_cache(self.k_new[i], self.v_new[i], self.slot_mapping, self.k_cache[i],
+                              self.v_cache[i], dev_err=self.dev_err, stream=stream)
+        ops.paged_attention_decode(self.out[i], self.q[i], self.k_cache[i], self.v_cache[i],
+                                   self.block_tables, self.context_lens, self.scale,
+                                   workspace=self.workspace, dev_err=self.dev_err, stream=stream)
+
+    def run(self, stream=None):
+        for i in range(self.num_layers):
+            self.run_layer(i, stream)
+        return self.out
+
+    def kernel_launches_per_step(self):
+        merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
+                                         self.batch.max_blocks) else 0
+        return self.num_layers * (2 + merge)
+
+    def check_errors(self):
+        code = ops.read_error_word(self.dev_err)
+        if code:
+            raise RuntimeError("device reported error code %d" % code)
+
+    # ---- end to end from host buffers -------------------------------------------
+    def host_buffers(self):
+        """Pinned host copies of the step inputs and an output buffer."""
+        if self._host is None:
+            pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+            self._host = {
+                "q": pin(self.q), "k_new": pin(self.k_new), "v_new": pin(self.v_new),
+                "slot_mapping": pin(self.slot_mapping), "block_tables": pin(self.block_tables),
+                "context_lens": pin(self.context_lens),
+                "out": torch.empty(self.out.shape, dtype=self.out.dtype, pin_memory=True),
+            }
+        return self._host
+
+    def host_bytes_per_step(self):
+        h = self.host_buffers()
+        up = sum(h[k].numel() * h[k].element_size()
+                 for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"))
+        return up, h["out"].numel() * h["out"].element_size()
+
+    def run_from_host(self, stream=None):
+        h = self.host_buffers()
+        s = torch.cuda.current_stream() if stream is None else stream
+        with torch.cuda.stream(s):
+            for name in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"):
+                getattr(self, name).copy_(h[name], non_blocking=True)
+            self.run(stream=s)
+            h["out"].copy_(self.out, non_blocking=True)
+        return h["out"]

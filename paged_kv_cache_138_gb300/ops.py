@@ -1,0 +1,145 @@
+"""Python face of the libpagedkv kernels: torch tensors in, C-ABI call out.
+
+Every function here only checks shapes and dtypes and marshals pointers; all
+computation runs in the CUDA kernels of libpagedkv.so.  Device tensors must be
+contiguous and live on the current CUDA device; work is enqueued on the current
+torch stream unless ``stream`` (a torch.cuda.Stream or raw handle) is given.
+"""
+import ctypes
+
+import torch
+
+from ._lib import check, lib
+
+HEAD_DIM = 128
+BLOCK_SIZE = 16
+
+
+def _stream_handle(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _dev(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got %s" % (name, ndim, tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t
+
+
+def new_error_word(device=None):
+    """A zeroed device int32 for the kernels' first-error code."""
+    return torch.zeros(1, dtype=torch.int32, device=device or torch.cuda.current_device())
+
+
+def read_error_word(dev_err):
+    """Synchronise and return the device error code (0 = none)."""
+    torch.cuda.current_stream().synchronize()
+    return int(dev_err.item())
+
+
+def workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, head_dim=HEAD_DIM):
+    return int(lib().pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
+                                                         max_blocks_per_seq, head_dim))
+
+
+def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None):
+    n = workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                           workspace=None, dev_err=None, stream=None):
+    """out[s,h] = softmax(scale * q[s,h] . K_s^T) V_s over context_lens[s] tokens."""
+    _dev(q, "q", torch.float16, 3)
+    _dev(out, "out", torch.float16, 3)
+    _dev(k_cache, "k_cache", torch.float16, 4)
+    _dev(v_cache, "v_cache", torch.float16, 4)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_cache.shape
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or D2 != D:
+        raise ValueError("shape mismatch")
+    if block_tables.shape[0] != S or context_lens.shape[0] != S:
+        raise ValueError("block_tables / context_lens must have num_seqs rows")
+    max_blocks = block_tables.shape[1]
+    need = workspace_bytes(S, Hq, max_blocks, D)
+    if need and workspace is None:
+        workspace = alloc_workspace(S, Hq, max_blocks, q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        S, Hq, Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes,
+        _ptr(dev_err), _stream_handle(stream))
+    check(rc, "paged_attention_decode")
+    return out
+
+
+def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, dev_err=None, stream=None):
+    """k_cache[slot // bs, slot % bs] = k[i] (and v) for slot = slot_mapping[i] >= 0."""
+    _dev(k, "k", torch.float16, 3)
+    _dev(v, "v", torch.float16, 3)
+    _dev(slot_mapping, "slot_mapping", torch.int64, 1)
+    _dev(k_cache, "k_cache", torch.float16, 4)
+    _dev(v_cache, "v_cache", torch.float16, 4)
+    T, Hkv, D = k.shape
+    nb, bs, Hkv2, D2 = k_cache.shape
+    if v.shape != k.shape or v_cache.shape != k_cache.shape or (Hkv2, D2) != (Hkv, D):
+        raise ValueError("shape mismatch")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    rc = lib().pkv_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
+                                     _ptr(v_cache), T, Hkv, D, bs, nb, _ptr(dev_err),
+                                     _stream_handle(stream))
+    check(rc, "reshape_and_cache")
+
+
+def slot_mapping(block_tables, positions, num_blocks, block_size=BLOCK_SIZE, out=None,
+                 dev_err=None, stream=None):
+    """slot[s] = table[s][p // bs] * bs + p % bs with p = positions[s] (device)."""
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(positions, "positions", torch.int32, 1)
+    S, mb = block_tables.shape
+    if out is None:
+        out = torch.empty(S, dtype=torch.int64, device=block_tables.device)
+    _dev(out, "out", torch.int64, 1)
+    rc = lib().pkv_slot_mapping(_ptr(block_tables), _ptr(positions), S, mb, block_size,
+                                int(num_blocks), _ptr(out), _ptr(dev_err), _stream_handle(stream))
+    check(rc, "slot_mapping")
+    return out
+
+
+def copy_blocks(k_caches, v_caches, block_pairs, dev_err=None, stream=None):
+    """cache[dst] = cache[src] for every (src, dst) row of block_pairs, every layer."""
+    if isinstance(k_caches, torch.Tensor):
+        k_caches, v_caches = [k_caches], [v_caches]
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("need matching, non-empty lists of K and V caches")
+    _dev(block_pairs, "block_pairs", torch.int64, 2)
+    ref = k_caches[0]
+    for c in list(k_caches) + list(v_caches):
+        _dev(c, "cache", ref.dtype)
+        if c.shape != ref.shape:
+            raise ValueError("all caches must share one shape")
+    n = len(k_caches)
+    kp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in k_caches])
+    vp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in v_caches])
+    block_bytes = ref[0].numel() * ref.element_size()
+    rc = lib().pkv_copy_blocks(kp, vp, n, _ptr(block_pairs), block_pairs.shape[0], block_bytes,
+                               ref.shape[0], _ptr(dev_err), _stream_handle(stream))
+    check(rc, "copy_blocks")

@@ -23,3 +23,20 @@ def load_golden(name):
 @pytest.fixture
 def golden():
     return load_golden
+
+
+@pytest.fixture(scope="session")
+def native_lib():
+    """Builds (if stale) and loads libpagedkv.so; no CUDA call is made."""
+    from paged_kv_cache_138_gb300 import build
+    build.build()
+    from paged_kv_cache_138_gb300 import _lib
+    return _lib.lib()
+
+
+def gpu_available():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False

@@ -1,0 +1,59 @@
+"""libpagedkv loads and exports every function include/pagedkv.h declares.
+
+No CUDA call is made here: argument validation that fails before any launch is
+exercised, nothing else.
+"""
+import ctypes
+import os
+import re
+
+from conftest import ROOT
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "pagedkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(native_lib):
+    from paged_kv_cache_138_gb300._lib import LIB_PATH, SIGNATURES
+    raw = ctypes.CDLL(LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 25
+    for n in names:
+        assert hasattr(raw, n), "missing export " + n
+        assert n in SIGNATURES, "binding lacks " + n
+
+
+def test_status_strings_and_version(native_lib):
+    assert native_lib.pkv_version() >= 100
+    assert native_lib.pkv_status_string(0) == b"ok"
+    assert b"out of KV blocks" in native_lib.pkv_status_string(-4)
+
+
+def test_host_side_validation_needs_no_gpu(native_lib):
+    L = native_lib
+    # unsupported head_dim / block size / GQA ratio are rejected before any launch
+    args = [None] * 6
+    assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 64, 16, 10, 4, 0.1, None, 0, None,
+                                        None) == -2
+    assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 128, 8, 10, 4, 0.1, None, 0, None,
+                                        None) == -2
+    assert L.pkv_paged_attention_decode(*args, 1, 12, 8, 128, 16, 10, 4, 0.1, None, 0, None,
+                                        None) == -2
+    assert L.pkv_paged_attention_decode(*args, 1, 24, 8, 128, 16, 10, 4, 0.1, None, 0, None,
+                                        None) == -2     # G = 3 has no kernel
+    # empty batch is a no-op
+    assert L.pkv_paged_attention_decode(*args, 0, 8, 8, 128, 16, 10, 4, 0.1, None, 0, None,
+                                        None) == 0
+    # workspace sizing: one split per 32 blocks, (D + 2) floats per split
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 32, 128) == 0
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 33, 128) == 4 * 8 * 2 * 130 * 4
+    assert L.pkv_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, None,
+                                   None) == 0
+    assert L.pkv_reshape_and_cache(None, None, None, None, None, 3, 8, 128, 16, 10, None,
+                                   None) == -1
+    assert L.pkv_copy_blocks(None, None, 1, None, 0, 4096, 10, None, None) == 0
+    assert L.pkv_copy_blocks(None, None, 1, None, 2, 4095, 10, None, None) == -1

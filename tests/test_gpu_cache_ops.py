@@ -1,0 +1,113 @@
+"""reshape_and_cache, slot mapping and copy_blocks on the GPU: bit-exact against
+the oracle's definitions.  Calls go through the C ABI (ops -> libpagedkv.so)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import cache_ops as oc
+from parity_helpers import oracle_batch
+from paged_kv_cache_138_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ops(native_lib):
+    from paged_kv_cache_138_gb300 import ops as o
+    return o
+
+
+def bits(t):
+    return t.cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("Hkv,nb,T", [(8, 64, 5), (40, 300, 64), (1, 7, 3), (32, 1000, 257)])
+def test_reshape_and_cache_bit_exact(ops, Hkv, nb, T):
+    rng = np.random.default_rng(Hkv * 1000 + T)
+    bs, D = 16, 128
+    kc = rng.standard_normal((nb, bs, Hkv, D)).astype(np.float16)
+    vc = rng.standard_normal((nb, bs, Hkv, D)).astype(np.float16)
+    k = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    v = rng.standard_normal((T, Hkv, D)).astype(np.float16)
+    slots = rng.choice(nb * bs, size=T, replace=False).astype(np.int64)
+    slots[::4] = -1                                   # skipped tokens
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    err = ops.new_error_word()
+    ops.reshape_and_cache(torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda(),
+                          torch.from_numpy(slots).cuda(), dk, dv, dev_err=err)
+    assert ops.read_error_word(err) == 0
+    oc.reshape_and_cache(k, v, slots, kc, vc)
+    assert np.array_equal(bits(dk), kc.view(np.uint16))
+    assert np.array_equal(bits(dv), vc.view(np.uint16))
+
+
+def test_reshape_and_cache_bad_slot_is_reported_and_skipped(ops):
+    nb, bs, H, D = 4, 16, 2, 128
+    kc = torch.zeros((nb, bs, H, D), dtype=torch.float16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = torch.ones((2, H, D), dtype=torch.float16, device="cuda")
+    slots = torch.tensor([nb * bs, 3], dtype=torch.int64, device="cuda")
+    err = ops.new_error_word()
+    ops.reshape_and_cache(k, k, slots, kc, vc, dev_err=err)
+    assert ops.read_error_word(err) == 3   # PKV_DEV_BAD_SLOT
+    flat = kc.view(nb * bs, H, D)
+    assert bool((flat[3] == 1).all()) and float(flat.sum()) == H * D
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_device_slot_mapping_matches_page_formula(ops, name):
+    w = wl.WORKLOADS[name]
+    tables, lens, slots, _, nb = oracle_batch(w)
+    err = ops.new_error_word()
+    got = ops.slot_mapping(torch.from_numpy(tables).cuda(), torch.from_numpy(lens - 1).cuda(), nb,
+                           dev_err=err)
+    assert ops.read_error_word(err) == 0
+    assert np.array_equal(got.cpu().numpy(), slots)
+
+
+def test_slot_mapping_edge_cases(ops):
+    tables = torch.tensor([[5, 2], [1, -1], [9, 0]], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([17, -1, 3], dtype=torch.int32, device="cuda")
+    err = ops.new_error_word()
+    got = ops.slot_mapping(tables, pos, num_blocks=8, dev_err=err)
+    assert got.cpu().tolist() == [2 * 16 + 1, -1, -1]
+    assert ops.read_error_word(err) == 1     # block 9 is outside the pool of 8
+    err = ops.new_error_word()
+    ops.slot_mapping(tables, torch.tensor([40, 0, 0], dtype=torch.int32, device="cuda"), 16,
+                     dev_err=err)
+    assert ops.read_error_word(err) == 5     # position past the table
+
+
+def test_copy_blocks_prefix_sharing_pairs(ops):
+    w = wl.WORKLOADS["prefix-sharing"]
+    _, _, _, pairs, nb = oracle_batch(w)
+    assert pairs.shape == (120, 2)
+    rng = np.random.default_rng(4)
+    shape = (nb, 16, 32, 128)
+    kc = rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    vc = rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    err = ops.new_error_word()
+    ops.copy_blocks(dk, dv, torch.from_numpy(pairs).cuda(), dev_err=err)
+    assert ops.read_error_word(err) == 0
+    oc.copy_blocks([kc], [vc], pairs)
+    assert np.array_equal(bits(dk), kc.view(np.uint16))
+    assert np.array_equal(bits(dv), vc.view(np.uint16))
+
+
+def test_copy_blocks_multi_layer_and_bad_pair(ops):
+    rng = np.random.default_rng(5)
+    layers = 3
+    shape = (10, 16, 4, 128)
+    ks = [rng.standard_normal(shape).astype(np.float16) for _ in range(layers)]
+    vs = [rng.standard_normal(shape).astype(np.float16) for _ in range(layers)]
+    dks = [torch.from_numpy(a).cuda() for a in ks]
+    dvs = [torch.from_numpy(a).cuda() for a in vs]
+    pairs = np.array([[1, 7], [3, 3], [12, 2], [4, 0]], dtype=np.int64)
+    err = ops.new_error_word()
+    ops.copy_blocks(dks, dvs, torch.from_numpy(pairs).cuda(), dev_err=err)
+    assert ops.read_error_word(err) == 1      # pair (12, 2) names a block past the pool
+    good = pairs[[0, 1, 3]]
+    oc.copy_blocks(ks, vs, good)
+    for a, d in zip(ks + vs, dks + dvs):
+        assert np.array_equal(bits(d), a.view(np.uint16))

@@ -1,0 +1,81 @@
+"""Every benchmark workload at its full size, run exactly as bench.py runs it
+(DecodeStep: copy_blocks for COW pairs, then per layer reshape_and_cache and
+paged attention), checked against the oracle.
+
+The oracle gets host copies of the caches taken BEFORE the step and applies its
+own copy_blocks and reshape_and_cache; nothing the GPU wrote is an oracle input.
+Small workloads are compared on every output row, large ones on seeded samples
+of rows the oracle evaluates one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import cache_ops as oc
+from parity_helpers import attention_tolerance, oracle_batch
+from paged_kv_cache_138_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = attention_tolerance()
+
+
+def run_and_check(name, layers_checked, rows_per_layer, all_rows=False):
+    from paged_kv_cache_138_gb300.engine import DecodeStep
+    from paged_kv_cache_138_gb300.scenario import prepare_batch
+    w = wl.WORKLOADS[name]
+    batch = prepare_batch(w)
+    tables, lens, slots, pairs, nb = oracle_batch(w)
+    assert np.array_equal(batch.block_tables, tables) and np.array_equal(batch.slot_mapping, slots)
+    step = DecodeStep(batch)
+    before = {i: (step.k_cache[i].cpu().numpy(), step.v_cache[i].cpu().numpy())
+              for i in layers_checked}
+    step.apply_cow()
+    out = step.run()
+    step.check_errors()
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(77)
+    S, Hq = batch.num_seqs, w.num_q_heads
+    worst = 0.0
+    for i in layers_checked:
+        kc, vc = before[i]
+        oc.copy_blocks([kc], [vc], pairs)
+        oc.reshape_and_cache(step.k_new[i].cpu().numpy(), step.v_new[i].cpu().numpy(), slots,
+                             kc, vc)
+        q = step.q[i].cpu().numpy()
+        gpu = out[i].cpu().numpy().astype(np.float64)
+        if all_rows:
+            ref = oa.paged_attention_decode(q, kc, vc, tables, lens, w.scale)
+            err = np.abs(gpu - ref)
+        else:
+            si = rng.integers(0, S, size=rows_per_layer).astype(np.int32)
+            hi = rng.integers(0, Hq, size=rows_per_layer).astype(np.int32)
+            si[:2] = [int(np.argmax(lens)), int(np.argmin(lens))]   # longest and shortest
+            ref = oa.paged_attention_decode_rows(q, kc, vc, tables, lens, w.scale, si, hi)
+            err = np.abs(gpu[si, hi] - ref)
+        assert np.isfinite(gpu).all()
+        worst = max(worst, float(err.max()))
+        # the new token's K/V landed at its slot, bit for bit
+        bs = w.block_size
+        for s in rng.integers(0, S, size=8):
+            b, o = divmod(int(slots[s]), bs)
+            assert np.array_equal(step.k_cache[i, b, o].cpu().numpy().view(np.uint16),
+                                  kc[b, o].view(np.uint16))
+    assert worst <= TOL, "max abs error %.3g" % worst
+    return worst
+
+
+def test_llama2_13b_layer_full_size(native_lib):
+    run_and_check("llama2-13b-layer", [0], 0, all_rows=True)
+
+
+def test_gqa_32_8_full_size(native_lib):
+    run_and_check("gqa-32-8", [0], 256)
+
+
+def test_prefix_sharing_full_size(native_lib):
+    run_and_check("prefix-sharing", [0], 0, all_rows=True)
+
+
+def test_llama2_7b_32_layer_full_size(native_lib):
+    run_and_check("llama2-7b-32layer", [0, 31], 96)
