@@ -44,10 +44,11 @@ class Workload:
     head_dim: int = HEAD_DIM
     block_size: int = BLOCK_SIZE
     description: str = ""
+    replica: int = 0     # independent copy of the workload (one per rank)
 
     @property
     def seed(self) -> int:
-        return 1000 + self.number
+        return 1000 + self.number + 7919 * self.replica
 
     @property
     def scale(self) -> float:
