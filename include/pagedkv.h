@@ -95,6 +95,34 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
 size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
                                            int max_blocks_per_seq, int head_dim);
 
+/*
+ * Allocation-free variant of pkv_paged_attention_decode.  The pages have no
+ * counterpart: it exists for callers that cannot allocate device memory, such
+ * as a plugin whose host framework owns the whole device memory pool, or code
+ * on a latency-critical path that must not take an allocation's implicit
+ * device synchronisation.  Same arguments and result as
+ * pkv_paged_attention_decode, minus the workspace: the split partials go to a
+ * fixed 16 MiB scratch array in this library's device memory, which every GPU
+ * that loads the library holds until the process exits.
+ *   - Returns PKV_ERR_UNSUPPORTED when the sizes need more scratch than the
+ *     array holds, i.e. when pkv_paged_attention_workspace_bytes(...) for the
+ *     same sizes exceeds 16 MiB (16777216 bytes).
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up the scratch array's device address
+ *     with that device current (cudaGetSymbolAddress); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array and leaves its contents behind; nothing
+ *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them.
+ */
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int64_t num_blocks,
+                                       int max_blocks_per_seq, float scale, int32_t* dev_err,
+                                       void* stream);
+
 /* ---- cache write --------------------------------------------------------- */
 /*
  * reshape_and_cache: store the K/V of new tokens at their slots.

@@ -471,3 +471,56 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     default: return launch<8>(mk, mv, p, st);
   }
 }
+
+// ---- allocation-free variant ------------------------------------------------------
+// Some callers cannot call cudaMalloc or any allocating routine: a plugin whose
+// host framework owns all device memory and hands out none, or code on a
+// latency-critical path where an allocation's implicit device synchronisation
+// is not acceptable.  For them the split partials live in a fixed scratch
+// array in this module's device memory instead of a caller workspace.
+namespace pkv {
+namespace attn {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+
+// Held by every device that loads this library, until the process exits.
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (host code may not use the symbol itself as a device pointer).
+void* static_scratch_ptr() {
+  static std::atomic<void*> ptrs[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* p = ptrs[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
+  ptrs[dev].store(p, std::memory_order_release);
+  return p;
+}
+
+}  // namespace attn
+}  // namespace pkv
+
+extern "C" int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                                  const void* v_cache,
+                                                  const int32_t* block_tables,
+                                                  const int32_t* context_lens, int num_seqs,
+                                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                                  int block_size, int64_t num_blocks,
+                                                  int max_blocks_per_seq, float scale,
+                                                  int32_t* dev_err, void* stream) {
+  using namespace pkv::attn;
+  const size_t need = pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
+                                                          max_blocks_per_seq, head_dim);
+  if (need > kStaticScratchBytes) return PKV_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (need > 0) {
+    scratch = static_scratch_ptr();
+    if (!scratch) return PKV_ERR_CUDA;
+  }
+  return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
+                                    num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    num_blocks, max_blocks_per_seq, scale, scratch,
+                                    need > 0 ? kStaticScratchBytes : 0, dev_err, stream);
+}
