@@ -47,18 +47,14 @@ constexpr int kHalfTileBytes = kBlockSize * 64 * 2;     // 16 rows x 128 B
 constexpr int kStageBytes = 4 * kHalfTileBytes;         // K lo, K hi, V lo, V hi
 constexpr float kRescaleThreshold = 8.0f;               // log2 units
 
-template <int G>
 struct Smem {
   static constexpr int stages = 0;
   static constexpr int stages_bytes = kWarps * kStages * kStageBytes;
-  static constexpr int q = stages + stages_bytes;                    // float [G][128]
-  static constexpr int p = q + G * kHeadDim * 4;                     // float [warps][16][G]
-  static constexpr int bars = p + kWarps * kBlockSize * G * 4;       // u64 [warps][stages]
-  static constexpr int table = bars + kWarps * kStages * 8;          // int32 [partition]
-  static constexpr int ml = table + kPartitionBlocks * 4;            // float [warps][G][2]
-  static constexpr int total = ml + kWarps * G * 2 * 4;
-  static constexpr int alloc = total + 1024;                         // alignment slack
-  static_assert(kWarps * G * kHeadDim * 4 <= stages_bytes, "merge buffer must fit");
+  static constexpr int bars = stages + stages_bytes;                  // u64 [warps][stages]
+  static constexpr int ml = bars + kWarps * kStages * 8;              // float [warps][8][2]
+  static constexpr int total = ml + kWarps * 8 * 2 * 4;
+  static constexpr int alloc = total + 1024;                          // alignment slack
+  static_assert(kWarps * 8 * kHeadDim * 4 <= stages_bytes, "merge buffer must fit");
 };
 
 struct Params {
@@ -84,93 +80,79 @@ __device__ __forceinline__ int clamp_context(const Params& p, int s, bool may_re
   return L;
 }
 
-template <int G>
-__device__ __forceinline__ void process_block(const uint8_t* st, const float* q_s, float* p_s,
-                                              int valid, int lane, float (&m)[G], float (&l)[G],
-                                              float2 (&o)[G][2]) {
+// Shared-memory byte offset of 16-byte chunk c (0..15 over the 128 dims) of
+// row `row` in a stage half pair starting at `base` (K: base 0, V: base 2):
+// each 64-dim half is a [16 rows x 128 B] TMA box with the 128-byte swizzle
+// (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t tile_chunk(uint32_t stage, int base, int row, int c) {
+  return stage + (base + (c >> 3)) * kHalfTileBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+}
+
+// One physical block (16 tokens) of one KV head for the G query heads of the
+// warp, on the tensor cores.  Rows of the 16-row MMA tile are query heads
+// (only the first G are real, the rest are zero), columns are tokens:
+//   S = Q K^T  : 8 k-steps over the 128 dims x 2 token halves  (16 MMAs)
+//   P = 2^(S * scale * log2 e - m), fp16                        (online softmax)
+//   O += P V   : 16 dim tiles of 8                              (16 MMAs)
+// Lane layout (m16n8k16): lane holds query row lane / 4; tokens
+// 2 * (lane % 4) + {0, 1} (+ 8); output dims 8 * nd + 2 * (lane % 4) + {0, 1}.
+__device__ __forceinline__ void process_block(uint32_t st, const uint32_t (&qa)[8][2], int valid,
+                                              int lane, float scale_log2, float& m, float& l,
+                                              float (&o)[16][4]) {
   constexpr unsigned kFull = 0xffffffffu;
-  const int t = lane & 15, half = lane >> 4;
-  // ---- scores: token t, dims [64*half, 64*half + 64) -----------------------
-  const uint8_t* krow = st + half * kHalfTileBytes + t * 128;
-  const int sw = t & 7;
-  float2 acc[G];
+  const int r8 = lane & 7, mi = lane >> 3;
+  // ---- S = Q K^T -------------------------------------------------------------
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  const int ktok = r8 + ((mi >> 1) << 3);  // matrices: (t0-7,lo) (t0-7,hi) (t8-15,lo) (t8-15,hi)
 #pragma unroll
-  for (int gi = 0; gi < G; ++gi) acc[gi] = make_float2(0.f, 0.f);
+  for (int kc = 0; kc < 8; ++kc) {
+    uint32_t b00, b01, b10, b11;
+    ldsm_x4(tile_chunk(st, 0, ktok, 2 * kc + (mi & 1)), b00, b01, b10, b11);
+    mma_16816_top(s0, qa[kc][0], qa[kc][1], b00, b01);
+    mma_16816_top(s1, qa[kc][0], qa[kc][1], b10, b11);
+  }
+  // ---- online softmax on this lane's row ------------------------------------------
+  const int tq = 2 * (lane & 3);
+  const float x0 = tq < valid ? s0[0] * scale_log2 : -INFINITY;
+  const float x1 = tq + 1 < valid ? s0[1] * scale_log2 : -INFINITY;
+  const float x2 = tq + 8 < valid ? s1[0] * scale_log2 : -INFINITY;
+  const float x3 = tq + 9 < valid ? s1[1] * scale_log2 : -INFINITY;
+  float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+  bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+  if (bm > m + kRescaleThreshold) {  // the 4 lanes of a row agree
+    const float alpha = exp2_approx(m - bm);
+    l *= alpha;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+      o[nd][0] *= alpha;
+      o[nd][1] *= alpha;
+    }
+    m = bm;
+  }
+  const float p0 = exp2_approx(x0 - m), p1 = exp2_approx(x1 - m);
+  const float p2 = exp2_approx(x2 - m), p3 = exp2_approx(x3 - m);
+  l += (p0 + p1) + (p2 + p3);
+  const uint32_t pa0 = pack_half2(p0, p1), pa2 = pack_half2(p2, p3);
+  // ---- rows past the context may hold anything (NaN): zero them, as 0 * NaN
+  // would poison the sums -------------------------------------------------------------
+  if (valid < kBlockSize) {
+    const int n = (kBlockSize - valid) * 16;  // 16-byte chunks to clear
+    for (int i = lane; i < n; i += 32) {
+      const int row = valid + (i >> 4), c = i & 15;
+      st_shared_zero16(st + (2 + (c >> 3)) * kHalfTileBytes + row * 128 + ((c & 7) << 4));
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+  }
+  // ---- O += P V ----------------------------------------------------------------------
+  const int vtok = r8 + ((mi & 1) << 3);  // matrices: (t0-7,c) (t8-15,c) (t0-7,c+1) (t8-15,c+1)
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(krow + ((j ^ sw) << 4));
-    const float2 k0 = half2_to_float2(raw.x), k1 = half2_to_float2(raw.y);
-    const float2 k2 = half2_to_float2(raw.z), k3 = half2_to_float2(raw.w);
-#pragma unroll
-    for (int gi = 0; gi < G; ++gi) {
-      const float4 qa = *reinterpret_cast<const float4*>(q_s + gi * kHeadDim + half * 64 + j * 8);
-      const float4 qb =
-          *reinterpret_cast<const float4*>(q_s + gi * kHeadDim + half * 64 + j * 8 + 4);
-      acc[gi] = ffma2(k0, make_float2(qa.x, qa.y), acc[gi]);
-      acc[gi] = ffma2(k1, make_float2(qa.z, qa.w), acc[gi]);
-      acc[gi] = ffma2(k2, make_float2(qb.x, qb.y), acc[gi]);
-      acc[gi] = ffma2(k3, make_float2(qb.z, qb.w), acc[gi]);
-    }
-  }
-  // ---- online softmax (base 2) -----------------------------------------------
-#pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    float sc = acc[gi].x + acc[gi].y;
-    sc += __shfl_xor_sync(kFull, sc, 16);
-    sc = t < valid ? sc : -INFINITY;
-    float bm = sc;
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 4));
-    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 8));
-    if (bm > m[gi] + kRescaleThreshold) {  // warp-uniform
-      const float alpha = exp2_approx(m[gi] - bm);
-      const float2 a2 = make_float2(alpha, alpha);
-      l[gi] *= alpha;
-      o[gi][0] = fmul2(o[gi][0], a2);
-      o[gi][1] = fmul2(o[gi][1], a2);
-      m[gi] = bm;
-    }
-    const float w = exp2_approx(sc - m[gi]);
-    float ws = w;
-    ws += __shfl_xor_sync(kFull, ws, 1);
-    ws += __shfl_xor_sync(kFull, ws, 2);
-    ws += __shfl_xor_sync(kFull, ws, 4);
-    ws += __shfl_xor_sync(kFull, ws, 8);
-    l[gi] += ws;
-    if (half == 0) p_s[t * G + gi] = w;
-  }
-  __syncwarp();
-  // ---- weighted values: lane owns dims [4*lane, 4*lane + 4) ------------------
-  const int hv = lane >> 4;
-  const int chunk = (lane & 15) >> 1;
-  const uint8_t* vbase = st + (2 + hv) * kHalfTileBytes + (lane & 1) * 8;
-#pragma unroll
-  for (int tt = 0; tt < kBlockSize; ++tt) {
-    if (tt < valid) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(vbase + tt * 128 + ((chunk ^ (tt & 7)) << 4));
-      const float2 v01 = half2_to_float2(raw.x), v23 = half2_to_float2(raw.y);
-      float w[G];
-      if constexpr (G % 4 == 0) {
-#pragma unroll
-        for (int gi = 0; gi < G; gi += 4) {
-          const float4 w4 = *reinterpret_cast<const float4*>(p_s + tt * G + gi);
-          w[gi] = w4.x; w[gi + 1] = w4.y; w[gi + 2] = w4.z; w[gi + 3] = w4.w;
-        }
-      } else if constexpr (G == 2) {
-        const float2 w2 = *reinterpret_cast<const float2*>(p_s + tt * G);
-        w[0] = w2.x; w[1] = w2.y;
-      } else {
-#pragma unroll
-        for (int gi = 0; gi < G; ++gi) w[gi] = p_s[tt * G + gi];
-      }
-#pragma unroll
-      for (int gi = 0; gi < G; ++gi) {
-        const float2 w2 = make_float2(w[gi], w[gi]);
-        o[gi][0] = ffma2(v01, w2, o[gi][0]);
-        o[gi][1] = ffma2(v23, w2, o[gi][1]);
-      }
-    }
+    uint32_t v0, v1, v2, v3;
+    ldsm_x4_trans(tile_chunk(st, 2, vtok, 2 * j + (mi >> 1)), v0, v1, v2, v3);
+    mma_16816_top(o[2 * j], pa0, pa2, v0, v1);
+    mma_16816_top(o[2 * j + 1], pa0, pa2, v2, v3);
   }
 }
 
@@ -178,7 +160,8 @@ template <int G>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
-  using SM = Smem<G>;
+  static_assert(G >= 1 && G <= 8, "query rows of the MMA tile");
+  constexpr unsigned kFull = 0xffffffffu;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 
@@ -200,40 +183,34 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int blk_begin = split * kPartitionBlocks;
   if (blk_begin >= nblk) return;
   const int n_here = min(kPartitionBlocks, nblk - blk_begin);
+  // warp w streams local blocks w, w + 4, ...; lane j holds the id of its j-th
+  const int my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
 
-  int32_t* tab = reinterpret_cast<int32_t*>(smem + SM::table);
-  float* q_s = reinterpret_cast<float*>(smem + SM::q);
-  float* p_s = reinterpret_cast<float*>(smem + SM::p) + warp * kBlockSize * G;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::bars) + warp * kStages;
-  uint8_t* ring = smem + SM::stages + warp * kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars) + warp * kStages;
+  const uint32_t ring = smem_u32(smem + Smem::stages + warp * kStages * kStageBytes);
 
-  if (threadIdx.x == 0) {
-    prefetch_tmap(&tmap_k);
-    prefetch_tmap(&tmap_v);
-  }
-  const int32_t* trow = p.block_tables + static_cast<int64_t>(s) * p.max_blocks + blk_begin;
-  for (int i = threadIdx.x; i < n_here; i += kThreads) {
-    int32_t b = __ldg(trow + i);
-    if (b < 0 || b >= p.num_blocks) {
+  int32_t my_id = -1;
+  if (lane < my_count) {
+    my_id = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + blk_begin + warp +
+                  lane * kWarps);
+    if (my_id < 0 || my_id >= p.num_blocks) {
       report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
-      b = -1;
+      my_id = -1;
     }
-    tab[i] = b;
   }
-  const __half* qp = p.q + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
-  for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads)
-    q_s[i] = __half2float(qp[i]) * p.scale_log2;
   if (lane == 0) {
+    if (warp == 0) {
+      prefetch_tmap(&tmap_k);
+      prefetch_tmap(&tmap_v);
+    }
     for (int j = 0; j < kStages; ++j) mbar_init(&bars[j], 1);
     fence_barrier_init();
   }
-  __syncthreads();
+  __syncwarp();
 
-  const int my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
-  auto issue = [&](int k) {  // lane 0 only: load local block k of this warp
-    const int32_t b = tab[warp + k * kWarps];
+  auto issue = [&](int k, int32_t b) {  // lane 0 only: local block k, physical id b
     uint64_t* bar = &bars[k % kStages];
-    uint8_t* st = ring + (k % kStages) * kStageBytes;
+    uint8_t* st = smem + Smem::stages + (warp * kStages + k % kStages) * kStageBytes;
     if (b < 0) {  // reported already: complete the phase without data
       mbar_arrive(bar);
       return;
@@ -247,60 +224,79 @@ __global__ void __launch_bounds__(kThreads, 2)
   };
 
   int issued = min(kStages, my_count);
-  if (lane == 0)
-    for (int k = 0; k < issued; ++k) issue(k);
-
-  float m[G], l[G];
-  float2 o[G][2];
 #pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    m[gi] = -INFINITY;
-    l[gi] = 0.f;
-    o[gi][0] = o[gi][1] = make_float2(0.f, 0.f);
+  for (int k = 0; k < kStages; ++k) {
+    const int32_t b = __shfl_sync(kFull, my_id, k);
+    if (lane == 0 && k < issued) issue(k, b);
   }
+
+  // q of this lane's row as m16n8k16 A fragments (raw fp16; scale applied to S)
+  uint32_t qa[8][2];
+  const int qrow = lane >> 2;
+  if (qrow < G) {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+        p.q + (static_cast<int64_t>(s) * Hq + h0 + qrow) * kHeadDim);
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) {
+      qa[kc][0] = __ldg(qp + 8 * kc + (lane & 3));
+      qa[kc][1] = __ldg(qp + 8 * kc + 4 + (lane & 3));
+    }
+  } else {
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) qa[kc][0] = qa[kc][1] = 0u;
+  }
+
+  float m = -INFINITY, l = 0.f;
+  float o[16][4];
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   bool ok = true;
   for (int k = 0; k < issued; ++k) {
     const int stage = k % kStages;
     const bool landed = mbar_wait_bounded(&bars[stage], (k / kStages) & 1, p.dev_err);
-    ok = __all_sync(0xffffffffu, ok && landed) != 0;
-    const int li = warp + k * kWarps;
-    if (ok && tab[li] >= 0) {
-      const int valid = min(kBlockSize, L - (blk_begin + li) * kBlockSize);
-      process_block<G>(ring + stage * kStageBytes, q_s, p_s, valid, lane, m, l, o);
+    ok = __all_sync(kFull, ok && landed) != 0;
+    const int32_t b = __shfl_sync(kFull, my_id, k);
+    if (ok && b >= 0) {
+      const int valid = min(kBlockSize, L - (blk_begin + warp + k * kWarps) * kBlockSize);
+      process_block(ring + stage * kStageBytes, qa, valid, lane, p.scale_log2, m, l, o);
     }
     __syncwarp();
+    const int32_t nb = __shfl_sync(kFull, my_id, issued < 32 ? issued : 0);
     if (ok && issued < my_count) {
-      if (lane == 0) issue(issued);
+      if (lane == 0) issue(issued, nb);
       ++issued;
     }
   }
+  l += __shfl_xor_sync(kFull, l, 1);
+  l += __shfl_xor_sync(kFull, l, 2);
 
   // ---- merge the 4 warps' partial softmax states ------------------------------
   __syncthreads();  // every issued tile has landed (or timed out); ring is free
-  float* ml = reinterpret_cast<float*>(smem + SM::ml);
-  float* ob = reinterpret_cast<float*>(smem + SM::stages);
-#pragma unroll
-  for (int gi = 0; gi < G; ++gi) {
-    if (lane == 0) {
-      ml[(warp * G + gi) * 2] = m[gi];
-      ml[(warp * G + gi) * 2 + 1] = l[gi];
+  float* ml = reinterpret_cast<float*>(smem + Smem::ml);
+  float* ob = reinterpret_cast<float*>(smem + Smem::stages);
+  if (qrow < G) {
+    if ((lane & 3) == 0) {
+      ml[(warp * 8 + qrow) * 2] = m;
+      ml[(warp * 8 + qrow) * 2 + 1] = l;
     }
-    *reinterpret_cast<float4*>(ob + (warp * G + gi) * kHeadDim + lane * 4) =
-        make_float4(o[gi][0].x, o[gi][0].y, o[gi][1].x, o[gi][1].y);
+    float* orow = ob + (warp * 8 + qrow) * kHeadDim + 2 * (lane & 3);
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd)
+      *reinterpret_cast<float2*>(orow + nd * 8) = make_float2(o[nd][0], o[nd][1]);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
     const int gi = e / kHeadDim, d = e % kHeadDim;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * G + gi) * 2]);
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + gi) * 2]);
     float num = 0.f, den = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float c = exp2_approx(ml[(w * G + gi) * 2] - M);
-        num += c * ob[(w * G + gi) * kHeadDim + d];
-        den += c * ml[(w * G + gi) * 2 + 1];
+        const float c = exp2_approx(ml[(w * 8 + gi) * 2] - M);
+        num += c * ob[(w * 8 + gi) * kHeadDim + d];
+        den += c * ml[(w * 8 + gi) * 2 + 1];
       }
     }
     const int64_t row = static_cast<int64_t>(s) * Hq + h0 + gi;
@@ -385,12 +381,12 @@ int launch(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, cudaSt
   if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(paged_attention_split_kernel<G>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<G>::alloc) != cudaSuccess)
+                             Smem::alloc) != cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev >= 0 && dev < 64) opted_in[dev].store(1, std::memory_order_release);
   }
   dim3 grid(p.num_kv_heads, p.num_seqs, p.max_splits);
-  paged_attention_split_kernel<G><<<grid, kThreads, Smem<G>::alloc, stream>>>(mk, mv, p);
+  paged_attention_split_kernel<G><<<grid, kThreads, Smem::alloc, stream>>>(mk, mv, p);
   if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   if (p.max_splits > 1) {
     paged_attention_merge_kernel<<<dim3(p.num_q_heads, p.num_seqs), kHeadDim, 0, stream>>>(p);
