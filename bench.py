@@ -321,6 +321,20 @@ def run_ours(args):
         e2e_ms = float(t.item())
     e2e_value = world * kv_bytes / (e2e_ms / 1e3) / 1e9
 
+    # ---- the same step replayed from a CUDA graph (one launch call per step) ---------
+    step.capture_graph()
+    for _ in range(3):
+        step.replay()
+    torch.cuda.synchronize(device)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        step.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(device)
+    step.check_errors()
+    graph_ms = g0.elapsed_time(g1) / args.steps
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -368,6 +382,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "graph": {"ms_per_step": graph_ms, "value": world * kv_bytes / (graph_ms / 1e3) / 1e9,
+                  "unit": "GB/s", "note": "same step replayed from a CUDA graph"},
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(),
     }

@@ -173,6 +173,29 @@ int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers
                     const int64_t* block_pairs, int num_pairs, int64_t block_bytes,
                     int64_t num_blocks, int32_t* dev_err, void* stream);
 
+/* ---- swap between pools ---------------------------------------------------- */
+/*
+ * swap_blocks: for every pair (src, dst) and every pool i,
+ *   dst_pools[i][dst] = src_pools[i][src]   (block_bytes bytes each)
+ * "qaqbuyan: vLLM PagedAttention", `_preempt_request`: a preempted request's KV
+ * blocks are copied from GPU memory to CPU memory (swap-out) and its GPU blocks
+ * freed; swap-in copies them back into freshly allocated blocks.  One kernel
+ * gathers the blocks, so either side may be host memory that the GPU can
+ * address: pinned (page-locked) and mapped, e.g. cudaHostAlloc or torch's
+ * pin_memory on a unified-address system.  The copy travels over the host link.
+ *   src_pools, dst_pools  HOST arrays of num_pools pointers (e.g. K and V of
+ *                         each layer), 16-byte aligned
+ *   block_pairs  int64 [num_pairs, 2] (src, dst), readable by the GPU; ids
+ *                outside [0, src_num_blocks) / [0, dst_num_blocks) are skipped
+ *                and reported as PKV_DEV_BAD_BLOCK_ID
+ *   block_bytes  bytes of one block of one pool, a multiple of 16
+ * Bit-exact.  Overlapping destinations race.
+ */
+int pkv_swap_blocks(const void* const* src_pools, void* const* dst_pools, int num_pools,
+                    const int64_t* block_pairs, int num_pairs, int64_t block_bytes,
+                    int64_t src_num_blocks, int64_t dst_num_blocks, int32_t* dev_err,
+                    void* stream);
+
 /* ---- host BlockManager ---------------------------------------------------- */
 /*
  * The BlockManager of "P06 BlockManager" (free list taken FIFO, reference

@@ -35,6 +35,7 @@ SIGNATURES = {
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P, _P]),
     "pkv_slot_mapping": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _P, _P]),
+    "pkv_swap_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pkv_bm_create": (_P, [_I64, _I, _I, _P]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_allocate": (_I, [_P, _I64, _P, _I64, _P, _I64, _P, _P]),

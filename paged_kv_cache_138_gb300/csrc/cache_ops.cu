@@ -165,3 +165,73 @@ extern "C" int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int
   }
   return PKV_OK;
 }
+
+// ---- swap_blocks: whole blocks between two pools --------------------------------------
+namespace pkv {
+namespace cache {
+
+struct PoolPtrs {
+  const uint4* src[kMaxLayersPerLaunch];
+  uint4* dst[kMaxLayersPerLaunch];
+};
+
+// grid (pairs, pools): one CTA copies one block of one pool.  Either side may be
+// host memory the GPU can address (pinned and mapped), which makes this the
+// device<->host swap of a preempted sequence's blocks.
+__global__ void __launch_bounds__(kThreads)
+    swap_blocks_kernel(const __grid_constant__ PoolPtrs ptrs, const int64_t* __restrict__ pairs,
+                       int64_t block_vecs, int64_t src_num_blocks, int64_t dst_num_blocks,
+                       int32_t* dev_err) {
+  const int pair = blockIdx.x, pool = blockIdx.y;
+  const int64_t src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
+  if (src < 0 || src >= src_num_blocks || dst < 0 || dst >= dst_num_blocks) {
+    if (threadIdx.x == 0 && pool == 0) report(dev_err, PKV_DEV_BAD_BLOCK_ID);
+    return;
+  }
+  const uint4* __restrict__ from = ptrs.src[pool] + src * block_vecs;
+  uint4* __restrict__ to = ptrs.dst[pool] + dst * block_vecs;
+  constexpr int kUnroll = 8;
+  int64_t i = threadIdx.x;
+  for (; i + (kUnroll - 1) * kThreads < block_vecs; i += kUnroll * kThreads) {
+    uint4 r[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) r[u] = from[i + u * kThreads];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) to[i + u * kThreads] = r[u];
+  }
+  for (; i < block_vecs; i += kThreads) to[i] = from[i];
+}
+
+}  // namespace cache
+}  // namespace pkv
+
+extern "C" int pkv_swap_blocks(const void* const* src_pools, void* const* dst_pools,
+                               int num_pools, const int64_t* block_pairs, int num_pairs,
+                               int64_t block_bytes, int64_t src_num_blocks,
+                               int64_t dst_num_blocks, int32_t* dev_err, void* stream) {
+  using namespace pkv::cache;
+  if (num_pools < 0 || num_pairs < 0 || block_bytes <= 0 || src_num_blocks <= 0 ||
+      dst_num_blocks <= 0 || block_bytes % 16 != 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_pools == 0 || num_pairs == 0) return PKV_OK;
+  if (!src_pools || !dst_pools || !block_pairs) return PKV_ERR_INVALID_ARG;
+  for (int base = 0; base < num_pools; base += kMaxLayersPerLaunch) {
+    const int n = std::min(kMaxLayersPerLaunch, num_pools - base);
+    PoolPtrs ptrs;
+    for (int i = 0; i < kMaxLayersPerLaunch; ++i) {
+      ptrs.src[i] = nullptr;
+      ptrs.dst[i] = nullptr;
+    }
+    for (int i = 0; i < n; ++i) {
+      const void* sp = src_pools[base + i];
+      void* dp = dst_pools[base + i];
+      if (!sp || !dp || !aligned16(sp) || !aligned16(dp)) return PKV_ERR_INVALID_ARG;
+      ptrs.src[i] = static_cast<const uint4*>(sp);
+      ptrs.dst[i] = static_cast<uint4*>(dp);
+    }
+    swap_blocks_kernel<<<dim3(num_pairs, n), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        ptrs, block_pairs, block_bytes / 16, src_num_blocks, dst_num_blocks, dev_err);
+    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}

@@ -73,6 +73,29 @@ class DecodeStep:
             self.run_layer(i, stream)
         return self.out
 
+    # ---- CUDA graph of one step ---------------------------------------------------
+    def capture_graph(self):
+        """Record one decode step (COW copies, then every layer) into a CUDA
+        graph; ``replay()`` then launches it with one call.  The step allocates
+        nothing, so the captured kernels reuse the buffers above."""
+        s = torch.cuda.Stream(self.device)
+        s.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(s):          # warm-up outside capture (one-time set-up)
+            self.apply_cow(s)
+            self.run(s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            self.apply_cow(s)
+            self.run(s)
+        torch.cuda.current_stream(self.device).wait_stream(s)
+        self.graph = g
+        return g
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
+
     def kernel_launches_per_step(self):
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
                                          self.batch.max_blocks) else 0

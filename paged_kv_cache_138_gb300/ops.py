@@ -143,3 +143,36 @@ def copy_blocks(k_caches, v_caches, block_pairs, dev_err=None, stream=None):
     rc = lib().pkv_copy_blocks(kp, vp, n, _ptr(block_pairs), block_pairs.shape[0], block_bytes,
                                ref.shape[0], _ptr(dev_err), _stream_handle(stream))
     check(rc, "copy_blocks")
+
+
+def swap_blocks(src_pools, dst_pools, block_pairs, dev_err=None, stream=None):
+    """dst_pools[i][dst] = src_pools[i][src] for every (src, dst) row of block_pairs.
+
+    Pools are tensors of one shape per side ([num_blocks, ...]); either side may
+    be pinned host memory (``tensor.is_pinned()``), which the kernel reads or
+    writes over the host link.  block_pairs must be readable by the GPU (a CUDA
+    tensor or pinned host memory)."""
+    if isinstance(src_pools, torch.Tensor):
+        src_pools, dst_pools = [src_pools], [dst_pools]
+    if len(src_pools) != len(dst_pools) or not src_pools:
+        raise ValueError("need matching, non-empty lists of source and destination pools")
+    for side in (src_pools, dst_pools):
+        for t in side:
+            if not (t.is_cuda or t.is_pinned()):
+                raise TypeError("pools must be CUDA tensors or pinned host tensors")
+            if not t.is_contiguous() or t.shape[1:] != side[0].shape[1:]:
+                raise ValueError("pools of one side must be contiguous with one shape")
+    if src_pools[0][0].numel() * src_pools[0].element_size() != \
+            dst_pools[0][0].numel() * dst_pools[0].element_size():
+        raise ValueError("source and destination blocks differ in size")
+    if block_pairs.dtype != torch.int64 or block_pairs.dim() != 2 or not \
+            (block_pairs.is_cuda or block_pairs.is_pinned()):
+        raise TypeError("block_pairs must be int64 [P, 2] on the GPU or pinned")
+    n = len(src_pools)
+    sp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in src_pools])
+    dp = (ctypes.c_void_p * n)(*[t.data_ptr() for t in dst_pools])
+    block_bytes = src_pools[0][0].numel() * src_pools[0].element_size()
+    rc = lib().pkv_swap_blocks(sp, dp, n, _ptr(block_pairs), block_pairs.shape[0], block_bytes,
+                               src_pools[0].shape[0], dst_pools[0].shape[0], _ptr(dev_err),
+                               _stream_handle(stream))
+    check(rc, "swap_blocks")

@@ -238,3 +238,72 @@ def decode_script(w: Workload, lengths) -> OpScript:
         cur += L
     sc.batch = list(range(len(lengths)))
     return sc
+
+
+# ---- content-keyed values for the multi-step driver ----------------------------------
+# A decode step's K/V for a token must be a function of the tokens before it (as
+# a model's would be), so that a block found again through the prefix cache
+# holds the same values a fresh prefill would write.  Each prefix gets a 64-bit
+# key (a multiply-xorshift chain over the token ids -- a random-number key, not
+# the BlockManager's block hash) that seeds NumPy's generator.
+
+_MIX = 0x9E3779B97F4A7C15
+_MASK = (1 << 64) - 1
+
+
+def prefix_keys(tokens, seed: int = 0) -> List[int]:
+    """Key of every prefix tokens[:j + 1], j = 0 .. n - 1."""
+    keys, h = [], (seed * _MIX + 0x632BE59BD9B4E019) & _MASK
+    for t in tokens:
+        h = ((h ^ (int(t) & 0xFFFFFFFF)) * _MIX) & _MASK
+        h ^= h >> 29
+        keys.append(h)
+    return keys
+
+
+def token_kv_host(keys, num_kv_heads: int, head_dim: int = HEAD_DIM):
+    """fp16 K and V rows [n, Hkv, D] of the tokens whose prefix keys are given."""
+    n = len(keys)
+    k = np.empty((n, num_kv_heads, head_dim), dtype=np.float16)
+    v = np.empty_like(k)
+    for i, key in enumerate(keys):
+        r = np.random.default_rng(key)
+        k[i] = host_normal_fp16(r, (num_kv_heads, head_dim))
+        v[i] = host_normal_fp16(r, (num_kv_heads, head_dim))
+    return k, v
+
+
+def step_query_host(seed: int, rid: int, pos: int, num_q_heads: int, head_dim: int = HEAD_DIM):
+    """fp16 query [Hq, D] of request ``rid`` decoding position ``pos``."""
+    return host_normal_fp16(np.random.default_rng([seed, rid, pos, 7]), (num_q_heads, head_dim))
+
+
+def next_token_host(seed: int, rid: int, pos: int, vocab: int = 32000) -> int:
+    """The token a request 'samples' at position ``pos`` (no model: random)."""
+    return int(np.random.default_rng([seed, rid, pos, 11]).integers(0, vocab))
+
+
+@dataclass
+class RequestSpec:
+    rid: int
+    prompt: List[int]
+    max_new_tokens: int
+    arrival_step: int = 0
+
+
+def serving_requests(seed: int, num_requests: int, num_system_prompts: int,
+                     system_prompt_len: int, suffix_max: int, new_min: int, new_max: int,
+                     arrivals_per_step: float = 0.0, vocab: int = 32000) -> List[RequestSpec]:
+    """Synthetic serving trace: each prompt is one of a few shared system prompts
+    followed by a private random suffix; output lengths ~U{new_min..new_max}."""
+    rng = np.random.default_rng([seed, 21])
+    systems = [rng.integers(0, vocab, size=system_prompt_len).tolist()
+               for _ in range(num_system_prompts)]
+    out = []
+    for rid in range(num_requests):
+        sys_p = systems[int(rng.integers(0, num_system_prompts))]
+        suffix = rng.integers(0, vocab, size=int(rng.integers(1, suffix_max + 1))).tolist()
+        arrive = int(rid / arrivals_per_step) if arrivals_per_step > 0 else 0
+        out.append(RequestSpec(rid, sys_p + suffix, int(rng.integers(new_min, new_max + 1)),
+                               arrive))
+    return out

@@ -111,3 +111,38 @@ def test_copy_blocks_multi_layer_and_bad_pair(ops):
     oc.copy_blocks(ks, vs, good)
     for a, d in zip(ks + vs, dks + dvs):
         assert np.array_equal(bits(d), a.view(np.uint16))
+
+
+def test_swap_blocks_device_host_round_trip(ops):
+    """swap-out to pinned host memory and swap-in to other device blocks, bit-exact
+    against the oracle's copy definition."""
+    rng = np.random.default_rng(8)
+    nb, hb = 40, 12
+    shape = (nb, 16, 4, 128)
+    kc = rng.standard_normal(shape).astype(np.float16)
+    vc = rng.standard_normal(shape).astype(np.float16)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    hk = torch.zeros((hb,) + shape[1:], dtype=torch.float16).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory()
+    out_pairs = np.array([[3, 0], [17, 5], [39, 11], [8, 2]], dtype=np.int64)
+    err = ops.new_error_word()
+    ops.swap_blocks([dk, dv], [hk, hv], torch.from_numpy(out_pairs).cuda(), dev_err=err)
+    assert ops.read_error_word(err) == 0
+    for src, dst in out_pairs:
+        assert np.array_equal(hk[dst].numpy().view(np.uint16), kc[src].view(np.uint16))
+        assert np.array_equal(hv[dst].numpy().view(np.uint16), vc[src].view(np.uint16))
+    in_pairs = np.array([[0, 20], [5, 21], [11, 3], [2, 39]], dtype=np.int64)
+    ops.swap_blocks([hk, hv], [dk, dv], torch.from_numpy(in_pairs).cuda(), dev_err=err)
+    assert ops.read_error_word(err) == 0
+    # the oracle's own host pools after the swap-out, then the swap-in
+    ek = np.zeros((hb,) + shape[1:], np.float16)
+    ev = np.zeros_like(ek)
+    for src, dst in out_pairs:
+        ek[dst], ev[dst] = kc[src], vc[src]
+    for src, dst in in_pairs:
+        kc[dst], vc[dst] = ek[src], ev[src]
+    assert np.array_equal(bits(dk), kc.view(np.uint16))
+    assert np.array_equal(bits(dv), vc.view(np.uint16))
+    bad = torch.tensor([[0, 1], [hb, 2]], dtype=torch.int64, device="cuda")
+    ops.swap_blocks([hk], [dk], bad, dev_err=err)
+    assert ops.read_error_word(err) == 1

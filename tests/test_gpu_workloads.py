@@ -79,3 +79,19 @@ def test_prefix_sharing_full_size(native_lib):
 
 def test_llama2_7b_32_layer_full_size(native_lib):
     run_and_check("llama2-7b-32layer", [0, 31], 96)
+
+
+def test_graph_replay_matches_eager(native_lib):
+    """One decode step captured in a CUDA graph gives the eager step's bits."""
+    from paged_kv_cache_138_gb300.engine import DecodeStep
+    from paged_kv_cache_138_gb300.scenario import prepare_batch
+    w = wl.WORKLOADS["prefix-sharing"]
+    step = DecodeStep(prepare_batch(w))
+    step.apply_cow()
+    eager = step.run().clone()
+    step.capture_graph()
+    step.out.zero_()
+    step.replay()
+    torch.cuda.synchronize()
+    step.check_errors()
+    assert torch.equal(step.out.view(torch.int16), eager.view(torch.int16))
