@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="llama2-13b-layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="tokens per KV block: 8, 16, 32 or 64")
     return ap.parse_args()
 
 
@@ -180,7 +182,12 @@ def setup(args, device, rank=0):
     from paged_kv_cache_138_gb300 import workloads as wl
     from paged_kv_cache_138_gb300.engine import DecodeStep
     from paged_kv_cache_138_gb300.scenario import prepare_batch
+    import dataclasses
     w = pd.replica(wl.WORKLOADS[args.workload], rank)
+    if args.block_size != w.block_size:
+        if args.workload == "prefix-sharing":
+            raise SystemExit("the prefix-sharing workload is defined for block size 16")
+        w = dataclasses.replace(w, block_size=args.block_size)
     batch = prepare_batch(w)
     step = DecodeStep(batch, device=device)
     return w, batch, step
@@ -374,6 +381,10 @@ def run_ours(args):
                    "block_size": w.block_size, "layers": w.num_layers,
                    "tokens": int(batch.context_lens.sum()), "kv_bytes_per_step": kv_bytes,
                    "pool_blocks": batch.num_blocks,
+                   "tail_waste_pct": 100.0 * float(sum(
+                       -(-int(L) // w.block_size) * w.block_size - int(L)
+                       for L in batch.context_lens)) / float(sum(
+                       -(-int(L) // w.block_size) * w.block_size for L in batch.context_lens)),
                    "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush"},
         "seq_steps_per_s": world * batch.num_seqs / (ms_per_step / 1e3),
         "pct_of_hbm_peak": {"measured": 100 * value / world / peak if peak_kind == "measured"
@@ -393,10 +404,123 @@ def run_ours(args):
     return 0
 
 
+def run_serving(args):
+    """Steady-state continuous batching (host BlockManager in the loop): a trace
+    of requests sharing 4 system prompts of 1024 tokens plus private suffixes,
+    64..512 new tokens each, decoded at batch <= 64 on the Llama-2-13B layer
+    shape.  Time covers whole steps: admissions, prefill writes, appends,
+    metadata copies, reshape_and_cache and attention."""
+    import torch
+
+    from paged_kv_cache_138_gb300 import workloads as wl
+    from paged_kv_cache_138_gb300.driver import ContinuousBatchDriver, DeviceSources
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    Hq = Hkv = 40
+    reqs = wl.serving_requests(2024, num_requests=4096, num_system_prompts=4,
+                               system_prompt_len=1024, suffix_max=512, new_min=64, new_max=512)
+    nb = 64 * 110
+    drv = ContinuousBatchDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
+                                sources=DeviceSources(7, Hq, Hkv), device=device)
+    for r in reqs:
+        drv.add_request(r.rid, r.prompt, r.max_new_tokens)
+    stats = {"seq_steps": 0, "kv_tokens": 0, "preempted": 0, "admitted": 0, "cached": 0,
+             "prefill": 0}
+    for _ in range(max(args.warmup, 3) * 20):
+        drv.step()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    steps = min(args.steps, 2000)
+    for _ in range(steps):
+        res = drv.step()
+        stats["seq_steps"] += len(res.rids)
+        stats["kv_tokens"] += res.kv_tokens
+        stats["preempted"] += len(res.preempted)
+        stats["admitted"] += len(res.admitted)
+        stats["cached"] += res.cached_tokens
+        stats["prefill"] += res.prefill_tokens
+    e1.record()
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    drv.check_errors()
+    kv_bytes = stats["kv_tokens"] * 2 * Hkv * 128 * 2
+    line = {"metric": METRIC, "value": kv_bytes / wall / 1e9, "unit": "GB/s", "n_gpus": 1,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
+            "config": {"workload": "serving", "description": run_serving.__doc__.split(".")[0],
+                       "max_batch": 64, "pool_blocks": nb, "heads": Hq},
+            "seq_steps_per_s": stats["seq_steps"] / wall,
+            "device_ms_per_step": e0.elapsed_time(e1) / steps, "stats": stats}
+    print(json.dumps(line))
+    return 0
+
+
+def run_swap(args):
+    """swap_blocks bandwidth over the host link: device pool -> pinned host pool
+    (swap-out) and back (swap-in), 1024 random blocks of K and V of the
+    Llama-2-7B shape (32 KV heads: 128 KiB per block per cache), against a
+    plain contiguous cudaMemcpy of the same bytes."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_138_gb300 import ops
+    device = torch.device("cuda", 0)
+    nb, hb, n = 4096, 2048, 1024
+    shape = (16, 32, 128)
+    k = torch.randn((nb,) + shape, device=device).half()
+    v = torch.randn((nb,) + shape, device=device).half()
+    hk = torch.empty((hb,) + shape, dtype=torch.float16, pin_memory=True)
+    hv = torch.empty_like(hk).pin_memory()
+    rng = np.random.default_rng(1)
+    out_pairs = torch.from_numpy(np.stack([rng.choice(nb, n, replace=False),
+                                           rng.choice(hb, n, replace=False)], 1)).to(device)
+    in_pairs = out_pairs[:, [1, 0]].contiguous()
+    err = ops.new_error_word(device)
+    nbytes = 2 * n * k[0].numel() * 2
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps / 1e3
+
+    reps = max(3, min(args.steps, 20))
+    t_out = timed(lambda: ops.swap_blocks([k, v], [hk, hv], out_pairs, dev_err=err), reps)
+    t_in = timed(lambda: ops.swap_blocks([hk, hv], [k, v], in_pairs, dev_err=err), reps)
+    flat_d = torch.empty(nbytes // 2, dtype=torch.float16, device=device)
+    flat_h = torch.empty(nbytes // 2, dtype=torch.float16, pin_memory=True)
+    t_ref_out = timed(lambda: flat_h.copy_(flat_d, non_blocking=True), reps)
+    t_ref_in = timed(lambda: flat_d.copy_(flat_h, non_blocking=True), reps)
+    assert ops.read_error_word(err) == 0
+    line = {"metric": "swap_blocks GB/s (device <-> pinned host)", "value": nbytes / t_out / 1e9,
+            "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": 3,
+            "ms_per_step": t_out * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bytes", "data": "synthetic",
+            "config": {"workload": "swap", "blocks": n, "bytes_per_direction": nbytes},
+            "swap_out_gbs": nbytes / t_out / 1e9, "swap_in_gbs": nbytes / t_in / 1e9,
+            "contiguous_memcpy_d2h_gbs": nbytes / t_ref_out / 1e9,
+            "contiguous_memcpy_h2d_gbs": nbytes / t_ref_in / 1e9}
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "serving":
+        return run_serving(args)
+    if args.workload == "swap":
+        return run_swap(args)
     return run_ours(args)
 
 

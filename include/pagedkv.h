@@ -16,7 +16,7 @@
  * has been synchronised.
  *
  * Terms (after "P06 BlockManager" and "ans20xx day 31"):
- *   block_size (bs)  tokens per physical KV block; the kernels here take 16
+ *   block_size (bs)  tokens per physical KV block (attention: 8, 16, 32 or 64)
  *   block table      int32 [num_seqs, max_blocks_per_seq]: logical block i of a
  *                    sequence is physical block table[s][i]
  *   slot             physical row of a token: table[pos / bs] * bs + pos % bs
@@ -36,7 +36,7 @@ extern "C" {
 /* ---- status codes (host return values) ---------------------------------- */
 #define PKV_OK 0
 #define PKV_ERR_INVALID_ARG (-1)   /* null pointer, negative size, misalignment */
-#define PKV_ERR_UNSUPPORTED (-2)   /* head_dim != 128, block_size != 16, bad GQA ratio */
+#define PKV_ERR_UNSUPPORTED (-2)   /* head_dim, block size or GQA ratio without a kernel */
 #define PKV_ERR_CUDA (-3)          /* a CUDA runtime/driver call failed */
 #define PKV_ERR_OUT_OF_BLOCKS (-4) /* BlockManager: no capacity; state unchanged */
 #define PKV_ERR_BAD_INDEX (-5)     /* unknown sequence, position outside a table */
@@ -63,18 +63,20 @@ int pkv_version(void);
  * the slot rule of "P06 BlockManager".  For every sequence s and query head h,
  * with g = h / (num_q_heads / num_kv_heads) and L = context_lens[s]:
  *   out[s, h, :] = sum_t softmax_t(scale * <q[s, h, :], K_s[t, g, :]>) V_s[t, g, :]
- * over exactly the L tokens t = 0 .. L-1, where K_s[t] is row t % 16 of
- * physical block block_tables[s][t / 16].  L == 0 gives a zero row.
+ * over exactly the L tokens t = 0 .. L-1, where K_s[t] is row t % bs of
+ * physical block block_tables[s][t / bs].  L == 0 gives a zero row.
  *
  *   out        fp16 [num_seqs, num_q_heads, head_dim], written
  *   q          fp16 [num_seqs, num_q_heads, head_dim]
  *   k_cache,
- *   v_cache    fp16 [num_blocks, 16, num_kv_heads, head_dim]; 16-byte aligned
+ *   v_cache    fp16 [num_blocks, block_size, num_kv_heads, head_dim]; 16-byte
+ *              aligned
  *   block_tables int32 [num_seqs, max_blocks_per_seq] (device)
  *   context_lens int32 [num_seqs] (device); tokens per sequence, the token
  *              written this step included
- *   head_dim must be 128, block_size 16, num_q_heads / num_kv_heads in
- *   {1, 2, 4, 8}; otherwise PKV_ERR_UNSUPPORTED.
+ *   head_dim must be 128, block_size one of 8, 16, 32, 64 and
+ *   num_q_heads / num_kv_heads one of 1, 2, 4, 8; otherwise PKV_ERR_UNSUPPORTED.
+ *   q must be 4-byte aligned.
  *   workspace  device scratch of at least
  *              pkv_paged_attention_workspace_bytes(...) bytes (may be NULL when
  *              that is 0); holds per-split partial results of long contexts.
@@ -91,9 +93,31 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                void* stream);
 
-/* Workspace bytes pkv_paged_attention_decode needs for these sizes (host only). */
+/* Workspace bytes pkv_paged_attention_decode needs for these sizes (host only;
+ * 0 when no sequence can span more than one split of 512 tokens). */
 size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
-                                           int max_blocks_per_seq, int head_dim);
+                                           int max_blocks_per_seq, int block_size,
+                                           int head_dim);
+
+/*
+ * Fused cache write + attention: one launch does what pkv_reshape_and_cache of
+ * the step's new tokens followed by pkv_paged_attention_decode does.  The new
+ * token of sequence s is its last one, position L - 1 (L = context_lens[s]);
+ * its slot is recomputed on the device from the block table
+ * (table[(L-1) / bs] * bs + (L-1) % bs, "P06 BlockManager"), k_new[s] / v_new[s]
+ * are stored there and used for that row of the attention.  Sequences with
+ * L == 0 write nothing.
+ *   k_new, v_new  fp16 [num_seqs, num_kv_heads, head_dim], 16-byte aligned
+ *   k_cache, v_cache are written (the new rows only)
+ * Other arguments, layouts and errors as pkv_paged_attention_decode.
+ */
+int pkv_paged_attention_decode_fused(void* out, const void* q, const void* k_new,
+                                     const void* v_new, void* k_cache, void* v_cache,
+                                     const int32_t* block_tables, const int32_t* context_lens,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks,
+                                     int max_blocks_per_seq, float scale, void* workspace,
+                                     size_t workspace_bytes, int32_t* dev_err, void* stream);
 
 /*
  * Allocation-free variant of pkv_paged_attention_decode.  The pages have no

@@ -29,7 +29,9 @@ SIGNATURES = {
     "pkv_version": (_I, []),
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I, _F,
                                         _P, _SZ, _P, _P]),
-    "pkv_paged_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "pkv_paged_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                              _I64, _I, _F, _P, _SZ, _P, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64,
                                                 _I, _F, _P, _P]),
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P, _P]),

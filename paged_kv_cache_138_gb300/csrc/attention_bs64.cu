@@ -1,0 +1,11 @@
+// Paged decode attention kernels for block size 64 (all GQA groups, with and
+// without the fused cache write).
+#include "attention_kernel.cuh"
+
+namespace pkv {
+namespace attn {
+
+PKV_DEFINE_LAUNCH_SPLIT(64)
+
+}  // namespace attn
+}  // namespace pkv

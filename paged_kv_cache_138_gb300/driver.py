@@ -90,7 +90,8 @@ class ContinuousBatchDriver:
         self.k_new = torch.empty((max_batch, num_kv_heads, head_dim), dtype=torch.float16,
                                  device=self.dev)
         self.v_new = torch.empty_like(self.k_new)
-        self.workspace = ops.alloc_workspace(max_batch, num_q_heads, max_blocks_per_seq, self.dev)
+        self.workspace = ops.alloc_workspace(max_batch, num_q_heads, max_blocks_per_seq, self.dev,
+                                             block_size)
         self.dev_err = ops.new_error_word(self.dev)
         if num_blocks < max_blocks_per_seq:
             raise ValueError("the pool must hold at least one full-length sequence")
@@ -250,12 +251,18 @@ class ContinuousBatchDriver:
         if B == 0:
             return res
         # new tokens' K/V and queries
-        for i, r in enumerate(batch):
-            pos = len(r.tokens) - 1
-            k, v = self.src.kv(r, [pos])
-            self.k_new[i].copy_(k[0])
-            self.v_new[i].copy_(v[0])
-            self.q[i].copy_(self.src.query(r, pos))
+        if hasattr(self.src, "decode_batch"):
+            k, v, q = self.src.decode_batch(batch)
+            self.k_new[:B].copy_(k)
+            self.v_new[:B].copy_(v)
+            self.q[:B].copy_(q)
+        else:
+            for i, r in enumerate(batch):
+                pos = len(r.tokens) - 1
+                k, v = self.src.kv(r, [pos])
+                self.k_new[i].copy_(k[0])
+                self.v_new[i].copy_(v[0])
+                self.q[i].copy_(self.src.query(r, pos))
         self._write_kv(self.k_new[:B], self.v_new[:B], slots)
         tables, lens = self.bm.block_tables([r.rid for r in batch], max_blocks=self.max_blocks)
         tables_d = torch.from_numpy(tables).to(self.dev, non_blocking=True)
@@ -319,3 +326,10 @@ class DeviceSources:
 
     def query(self, req, pos):
         return torch.randn((self.Hq, self.D), generator=self.gen, device=self.dev).half()
+
+    def decode_batch(self, batch):
+        B = len(batch)
+        k = torch.randn((B, self.Hkv, self.D), generator=self.gen, device=self.dev).half()
+        v = torch.randn((B, self.Hkv, self.D), generator=self.gen, device=self.dev).half()
+        q = torch.randn((B, self.Hq, self.D), generator=self.gen, device=self.dev).half()
+        return k, v, q

@@ -48,7 +48,7 @@ class DecodeStep:
         self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(dev)
         self.cow_pairs = torch.from_numpy(batch.cow_pairs).to(dev)
         self.out = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
-        self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev)
+        self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev, bs)
         self.dev_err = ops.new_error_word(dev)
         self._host = None
 
@@ -98,7 +98,8 @@ class DecodeStep:
 
     def kernel_launches_per_step(self):
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
-                                         self.batch.max_blocks) else 0
+                                         self.batch.max_blocks,
+                                         self.batch.workload.block_size) else 0
         return self.num_layers * (2 + merge)
 
     def check_errors(self):

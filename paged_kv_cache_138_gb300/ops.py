@@ -50,13 +50,16 @@ def read_error_word(dev_err):
     return int(dev_err.item())
 
 
-def workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, head_dim=HEAD_DIM):
+def workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size=BLOCK_SIZE,
+                    head_dim=HEAD_DIM):
     return int(lib().pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
-                                                         max_blocks_per_seq, head_dim))
+                                                         max_blocks_per_seq, block_size,
+                                                         head_dim))
 
 
-def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None):
-    n = workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq)
+def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None,
+                    block_size=BLOCK_SIZE):
+    n = workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size)
     if n == 0:
         return None
     return torch.empty(n, dtype=torch.uint8, device=device or torch.cuda.current_device())
@@ -78,15 +81,46 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     if block_tables.shape[0] != S or context_lens.shape[0] != S:
         raise ValueError("block_tables / context_lens must have num_seqs rows")
     max_blocks = block_tables.shape[1]
-    need = workspace_bytes(S, Hq, max_blocks, D)
+    need = workspace_bytes(S, Hq, max_blocks, bs, D)
     if need and workspace is None:
-        workspace = alloc_workspace(S, Hq, max_blocks, q.device)
+        workspace = alloc_workspace(S, Hq, max_blocks, q.device, bs)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().pkv_paged_attention_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         S, Hq, Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes,
         _ptr(dev_err), _stream_handle(stream))
     check(rc, "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                 context_lens, scale, workspace=None, dev_err=None, stream=None):
+    """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
+    sequence (slot from its block table) and attend over context_lens[s] tokens."""
+    _dev(q, "q", torch.float16, 3)
+    _dev(out, "out", torch.float16, 3)
+    _dev(k_new, "k_new", torch.float16, 3)
+    _dev(v_new, "v_new", torch.float16, 3)
+    _dev(k_cache, "k_cache", torch.float16, 4)
+    _dev(v_cache, "v_cache", torch.float16, 4)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, D2 = k_cache.shape
+    if out.shape != q.shape or v_cache.shape != k_cache.shape or D2 != D:
+        raise ValueError("shape mismatch")
+    if k_new.shape != (S, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    max_blocks = block_tables.shape[1]
+    need = workspace_bytes(S, Hq, max_blocks, bs, D)
+    if need and workspace is None:
+        workspace = alloc_workspace(S, Hq, max_blocks, q.device, bs)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_decode_fused(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), S, Hq, Hkv, D, bs, nb, max_blocks, float(scale),
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream_handle(stream))
+    check(rc, "paged_attention_decode_fused")
     return out
 
 

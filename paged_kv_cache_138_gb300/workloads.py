@@ -94,16 +94,18 @@ def context_lengths(w: Workload) -> np.ndarray:
 
 def pool_blocks(w: Workload, lengths: Optional[np.ndarray] = None) -> int:
     """Physical blocks in the pool for workload ``w``."""
-    if w.name == "tiny":
+    if w.name == "tiny" and w.block_size == BLOCK_SIZE:
         return 64
     if w.name == "llama2-7b-32layer":
-        return w.num_seqs * blocks_for(4096)
+        return w.num_seqs * blocks_for(4096, w.block_size)
     if w.name == "prefix-sharing":
         p = prefix_sharing_private_tokens(w)
         unique = 8 * blocks_for(2048) + sum(blocks_for(1 + int(x)) for x in p)
         return int(np.ceil(1.1 * unique))
+    if w.name == "tiny" and w.block_size != BLOCK_SIZE:
+        return 64 * BLOCK_SIZE // w.block_size
     lengths = context_lengths(w) if lengths is None else lengths
-    return int(np.ceil(1.1 * sum(blocks_for(int(L)) for L in lengths)))
+    return int(np.ceil(1.1 * sum(blocks_for(int(L), w.block_size) for L in lengths)))
 
 
 def free_order(w: Workload, num_blocks: Optional[int] = None) -> np.ndarray:

@@ -39,7 +39,7 @@ def test_host_side_validation_needs_no_gpu(native_lib):
     args = [None] * 6
     assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 64, 16, 10, 4, 0.1, None, 0, None,
                                         None) == -2
-    assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 128, 8, 10, 4, 0.1, None, 0, None,
+    assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 128, 12, 10, 4, 0.1, None, 0, None,
                                         None) == -2
     assert L.pkv_paged_attention_decode(*args, 1, 12, 8, 128, 16, 10, 4, 0.1, None, 0, None,
                                         None) == -2
@@ -48,9 +48,16 @@ def test_host_side_validation_needs_no_gpu(native_lib):
     # empty batch is a no-op
     assert L.pkv_paged_attention_decode(*args, 0, 8, 8, 128, 16, 10, 4, 0.1, None, 0, None,
                                         None) == 0
-    # workspace sizing: one split per 32 blocks, (D + 2) floats per split
-    assert L.pkv_paged_attention_workspace_bytes(4, 8, 32, 128) == 0
-    assert L.pkv_paged_attention_workspace_bytes(4, 8, 33, 128) == 4 * 8 * 2 * 130 * 4
+    # workspace sizing: one split per 512 tokens, (D + 2) floats per split
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 32, 16, 128) == 0
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 33, 16, 128) == 4 * 8 * 2 * 130 * 4
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 64, 8, 128) == 0
+    assert L.pkv_paged_attention_workspace_bytes(4, 8, 9, 64, 128) == 4 * 8 * 2 * 130 * 4
+    # block sizes without a kernel
+    assert L.pkv_paged_attention_decode(*args, 1, 8, 8, 128, 4, 10, 4, 0.1, None, 0, None,
+                                        None) == -2
+    assert L.pkv_paged_attention_decode_fused(*(args + [None, None]), 1, 8, 8, 128, 128, 10, 4,
+                                              0.1, None, 0, None, None) == -2
     assert L.pkv_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, None,
                                    None) == 0
     assert L.pkv_reshape_and_cache(None, None, None, None, None, 3, 8, 128, 16, 10, None,
