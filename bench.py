@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default="llama2-13b-layer")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--unfused", action="store_true",
+                    help="separate reshape_and_cache and attention launches per layer")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per KV block: 8, 16, 32 or 64")
     return ap.parse_args()
@@ -75,7 +77,7 @@ def traffic_record(kernel_key):
     try:
         with open(path) as f:
             rec = json.load(f).get(kernel_key)
-        src = os.path.join(ROOT, "paged_kv_cache_138_gb300", "csrc", "paged_attention.cu")
+        src = os.path.join(ROOT, "paged_kv_cache_138_gb300", "csrc", "attention_kernel.cuh")
         digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         if rec and rec.get("source_sha256_16") == digest:
             return rec
@@ -189,7 +191,7 @@ def setup(args, device, rank=0):
             raise SystemExit("the prefix-sharing workload is defined for block size 16")
         w = dataclasses.replace(w, block_size=args.block_size)
     batch = prepare_batch(w)
-    step = DecodeStep(batch, device=device)
+    step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False))
     return w, batch, step
 
 
@@ -281,14 +283,22 @@ def run_ours(args):
         for _ in range(args.steps):
             step.apply_cow(stream)
             for i in range(step.num_layers):
-                ops.reshape_and_cache(step.k_new[i], step.v_new[i], step.slot_mapping,
-                                      step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
-                                      stream=stream)
+                if not step.fused:
+                    ops.reshape_and_cache(step.k_new[i], step.v_new[i], step.slot_mapping,
+                                          step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
+                                          stream=stream)
                 attn_events[k][0].record(stream)
-                ops.paged_attention_decode(step.out[i], step.q[i], step.k_cache[i],
-                                           step.v_cache[i], step.block_tables, step.context_lens,
-                                           step.scale, workspace=step.workspace,
-                                           dev_err=step.dev_err, stream=stream)
+                if step.fused:
+                    ops.paged_attention_decode_fused(
+                        step.out[i], step.q[i], step.k_new[i], step.v_new[i], step.k_cache[i],
+                        step.v_cache[i], step.block_tables, step.context_lens, step.scale,
+                        workspace=step.workspace, dev_err=step.dev_err, stream=stream)
+                else:
+                    ops.paged_attention_decode(step.out[i], step.q[i], step.k_cache[i],
+                                               step.v_cache[i], step.block_tables,
+                                               step.context_lens, step.scale,
+                                               workspace=step.workspace, dev_err=step.dev_err,
+                                               stream=stream)
                 attn_events[k][1].record(stream)
                 k += 1
         stop.record(stream)
@@ -350,12 +360,15 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     layer_kv = kv_bytes / w.num_layers
     achieved = layer_kv / (attn_ms / 1e3) / 1e9
-    tr = traffic_record("paged_attention_decode/" + args.workload)
+    tr = traffic_record(("fused/" if step.fused else "") + "paged_attention_decode/" +
+                        args.workload + ("" if w.block_size == 16 else "/bs%d" % w.block_size))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "algorithmic_bytes_per_launch": layer_kv,
-                "kernel": "paged_attention_decode (split kernel + LSE merge, CUDA events)",
+                "kernel": ("paged_attention_decode_fused (cache write + split kernel + LSE "
+                           "merge, CUDA events)" if step.fused else
+                           "paged_attention_decode (split kernel + LSE merge, CUDA events)"),
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
     cpu = None
     if not args.no_cpu_baseline:
@@ -376,6 +389,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 (fp32 accumulate)",
         "data": "synthetic",
         "config": {"workload": args.workload, "description": w.description,
+                   "fused_cache_write": step.fused,
                    "num_seqs": batch.num_seqs, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "layers": w.num_layers,

@@ -17,9 +17,13 @@ from .scenario import DecodeBatch
 
 
 class DecodeStep:
-    def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None):
+    def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None,
+                 fused=False):
         """host_values: None draws q/K/V on the device (torch generator seeded by
-        the workload); otherwise the tuple of ``workloads.host_tensors`` (numpy)."""
+        the workload); otherwise the tuple of ``workloads.host_tensors`` (numpy).
+        fused: each layer is one launch of the fused cache-write + attention
+        kernel instead of reshape_and_cache followed by attention."""
+        self.fused = bool(fused)
         w = batch.workload
         self.batch = batch
         self.device = torch.device(device or "cuda")
@@ -62,6 +66,12 @@ class DecodeStep:
                         self.cow_pairs, dev_err=self.dev_err, stream=stream)
 
     def run_layer(self, i, stream=None):
+        if self.fused:
+            ops.paged_attention_decode_fused(
+                self.out[i], self.q[i], self.k_new[i], self.v_new[i], self.k_cache[i],
+                self.v_cache[i], self.block_tables, self.context_lens, self.scale,
+                workspace=self.workspace, dev_err=self.dev_err, stream=stream)
+            return
         ops.reshape_and_cache(self.k_new[i], self.v_new[i], self.slot_mapping, self.k_cache[i],
                               self.v_cache[i], dev_err=self.dev_err, stream=stream)
         ops.paged_attention_decode(self.out[i], self.q[i], self.k_cache[i], self.v_cache[i],
@@ -100,7 +110,7 @@ class DecodeStep:
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
                                          self.batch.max_blocks,
                                          self.batch.workload.block_size) else 0
-        return self.num_layers * (2 + merge)
+        return self.num_layers * ((1 if self.fused else 2) + merge)
 
     def check_errors(self):
         code = ops.read_error_word(self.dev_err)

@@ -7,6 +7,9 @@ own copy_blocks and reshape_and_cache; nothing the GPU wrote is an oracle input.
 Small workloads are compared on every output row, large ones on seeded samples
 of rows the oracle evaluates one by one.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -61,6 +64,12 @@ def run_and_check(name, layers_checked, rows_per_layer, all_rows=False):
             b, o = divmod(int(slots[s]), bs)
             assert np.array_equal(step.k_cache[i, b, o].cpu().numpy().view(np.uint16),
                                   kc[b, o].view(np.uint16))
+    report = os.environ.get("PKV_PARITY_REPORT")
+    if report:
+        with open(report, "a") as f:
+            f.write(json.dumps({"workload": name, "max_abs_err": worst, "tol": TOL,
+                                "rows": "all" if all_rows else rows_per_layer,
+                                "layers": list(layers_checked)}) + "\n")
     assert worst <= TOL, "max abs error %.3g" % worst
     return worst
 
