@@ -4,6 +4,9 @@ Tolerance: max |out_gpu - out_oracle| <= 2e-3 on fp16 outputs (fp16 inputs,
 fp32 accumulation on the GPU, one fp16 rounding of the result).  Calls go
 through the C ABI (ops -> libpagedkv.so).
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -145,6 +148,12 @@ def test_tiny_workload_full_step(ops):
     q, k_new, v_new, kc, vc = [a.copy() for a in hv]
     oc.reshape_and_cache(k_new[0], v_new[0], slots, kc[0], vc[0])
     ref = oa.paged_attention_decode(q[0], kc[0], vc[0], tables, lens, w.scale)
+    report = os.environ.get("PKV_PARITY_REPORT")
+    if report:
+        err = float(np.abs(out[0].cpu().numpy().astype(np.float64) - ref).max())
+        with open(report, "a") as f:
+            f.write(json.dumps({"workload": "tiny", "max_abs_err": err, "tol": TOL,
+                                "rows": "all", "layers": [0]}) + "\n")
     assert_close(out[0].cpu().numpy(), ref)
     # the cache now holds each new token at its slot
     assert np.array_equal(step.k_cache.cpu().numpy().view(np.uint16), kc.view(np.uint16))
