@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--unfused", action="store_true",
                     help="separate reshape_and_cache and attention launches per layer")
+    ap.add_argument("--grouped", choices=["auto", "on", "off"], default="auto",
+                    help="shared-prefix grouped attention (auto: on for prefix-sharing)")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per KV block: 8, 16, 32 or 64")
     return ap.parse_args()
@@ -191,7 +193,10 @@ def setup(args, device, rank=0):
             raise SystemExit("the prefix-sharing workload is defined for block size 16")
         w = dataclasses.replace(w, block_size=args.block_size)
     batch = prepare_batch(w)
-    step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False))
+    grouped = {"on": True, "off": False}.get(getattr(args, "grouped", "auto"),
+                                              args.workload == "prefix-sharing")
+    step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False),
+                      grouped=grouped)
     return w, batch, step
 
 
@@ -288,7 +293,13 @@ def run_ours(args):
                                           step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
                                           stream=stream)
                 attn_events[k][0].record(stream)
-                if step.fused:
+                if step.groups is not None:
+                    gf, sg, gs, mx = step.groups
+                    ops.paged_attention_decode_grouped(
+                        step.out[i], step.q[i], step.k_cache[i], step.v_cache[i],
+                        step.block_tables, step.context_lens, gf, sg, gs, mx, step.scale,
+                        workspace=step.workspace, dev_err=step.dev_err, stream=stream)
+                elif step.fused:
                     ops.paged_attention_decode_fused(
                         step.out[i], step.q[i], step.k_new[i], step.v_new[i], step.k_cache[i],
                         step.v_cache[i], step.block_tables, step.context_lens, step.scale,
@@ -359,6 +370,13 @@ def run_ours(args):
 
     peak, peak_kind = hbm_peak()
     layer_kv = kv_bytes / w.num_layers
+    unique_kv = None
+    if args.workload == "prefix-sharing":
+        # forked samples share prompt blocks: the roofline counts each distinct
+        # (block, row) once -- what HBM must deliver at minimum
+        unique_kv = accounting.unique_kv_bytes(batch.block_tables, batch.context_lens,
+                                               w.block_size, w.num_kv_heads, w.head_dim)
+        layer_kv = unique_kv
     achieved = layer_kv / (attn_ms / 1e3) / 1e9
     tr = traffic_record(("fused/" if step.fused else "") + "paged_attention_decode/" +
                         args.workload + ("" if w.block_size == 16 else "/bs%d" % w.block_size))
@@ -390,10 +408,12 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": args.workload, "description": w.description,
                    "fused_cache_write": step.fused,
+                   "grouped_shared_prefix": step.groups is not None,
                    "num_seqs": batch.num_seqs, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                    "block_size": w.block_size, "layers": w.num_layers,
                    "tokens": int(batch.context_lens.sum()), "kv_bytes_per_step": kv_bytes,
+                   "unique_kv_bytes_per_step": unique_kv,
                    "pool_blocks": batch.num_blocks,
                    "tail_waste_pct": 100.0 * float(sum(
                        -(-int(L) // w.block_size) * w.block_size - int(L)

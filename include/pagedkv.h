@@ -48,6 +48,8 @@ extern "C" {
 #define PKV_DEV_BAD_SLOT 3         /* slot >= num_blocks * block_size */
 #define PKV_DEV_WAIT_TIMEOUT 4     /* a bounded wait on a copy gave up */
 #define PKV_DEV_BAD_POSITION 5     /* position outside its block table */
+#define PKV_DEV_BAD_GROUP 6        /* a shared-prefix group whose members do not
+                                      share the stated blocks, or too many rows */
 
 /* Human-readable name of a status code (static string). */
 const char* pkv_status_string(int status);
@@ -146,6 +148,41 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        int block_size, int64_t num_blocks,
                                        int max_blocks_per_seq, float scale, int32_t* dev_err,
                                        void* stream);
+
+/*
+ * Grouped decode attention for sequences that share a prefix (forked samples
+ * of one prompt, "ans20xx day 31" `fork_sequence`; prefix-cache hits, "P06
+ * BlockManager").  Same result as pkv_paged_attention_decode on the same
+ * arguments; the grouping only changes how the work is done: the prefix a
+ * group shares is read from HBM once for all its members instead of once per
+ * member.
+ *   group_first   int32 [num_groups + 1] (device): group i is the sequences
+ *                 group_first[i] .. group_first[i+1] - 1 (contiguous, covering
+ *                 0 .. num_seqs - 1 in order)
+ *   seq_group     int32 [num_seqs] (device): the group of each sequence
+ *   group_shared  int32 [num_groups] (device): tokens every member holds through
+ *                 the same physical blocks as the group's first member; a
+ *                 multiple of 16 and of block_size, <= every member's context
+ *                 length, <= max_shared_tokens; 0 for no sharing.  Members x
+ *                 (num_q_heads / num_kv_heads) must be <= 16.  Violations are
+ *                 reported as PKV_DEV_BAD_GROUP.
+ *   workspace     at least pkv_paged_attention_grouped_workspace_bytes(...)
+ * The new tokens must already be in the cache (pkv_reshape_and_cache).
+ */
+int pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       const int32_t* context_lens, const int32_t* group_first,
+                                       const int32_t* seq_group, const int32_t* group_shared,
+                                       int num_groups, int max_shared_tokens, int num_seqs,
+                                       int num_q_heads, int num_kv_heads, int head_dim,
+                                       int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                                       float scale, void* workspace, size_t workspace_bytes,
+                                       int32_t* dev_err, void* stream);
+
+/* Workspace bytes pkv_paged_attention_decode_grouped needs (host only). */
+size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads,
+                                                   int max_blocks_per_seq, int block_size,
+                                                   int head_dim, int max_shared_tokens);
 
 /* ---- cache write --------------------------------------------------------- */
 /*

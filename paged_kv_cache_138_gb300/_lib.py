@@ -21,6 +21,7 @@ PKV_DEV_BAD_CONTEXT_LEN = 2
 PKV_DEV_BAD_SLOT = 3
 PKV_DEV_WAIT_TIMEOUT = 4
 PKV_DEV_BAD_POSITION = 5
+PKV_DEV_BAD_GROUP = 6
 
 # name -> (restype, argtypes); every symbol the header declares.
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -30,6 +31,9 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I, _F,
                                         _P, _SZ, _P, _P]),
     "pkv_paged_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_decode_grouped": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                                                _I, _I, _I, _I64, _I, _F, _P, _SZ, _P, _P]),
+    "pkv_paged_attention_grouped_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "pkv_paged_attention_decode_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                               _I64, _I, _F, _P, _SZ, _P, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64,

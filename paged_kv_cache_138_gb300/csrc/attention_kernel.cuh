@@ -54,10 +54,10 @@ struct Smem {
   static constexpr int stages = 0;
   static constexpr int stages_bytes = kWarps * kStages * kStageBytes;
   static constexpr int bars = stages + stages_bytes;                  // u64 [warps][stages]
-  static constexpr int ml = bars + kWarps * kStages * 8;              // float [warps][8][2]
-  static constexpr int total = ml + kWarps * 8 * 2 * 4;
+  static constexpr int ml = bars + kWarps * kStages * 8;              // float [warps][16][2]
+  static constexpr int total = ml + kWarps * 16 * 2 * 4;
   static constexpr int alloc = total + 1024;                          // alignment slack
-  static_assert(kWarps * 8 * kHeadDim * 4 <= stages_bytes, "merge buffer must fit");
+  static_assert(kWarps * 16 * kHeadDim * 4 <= stages_bytes, "merge buffer must fit");
 };
 
 struct Params {
@@ -73,14 +73,28 @@ struct Params {
   const __half* v_new;
   __half* k_cache;      // [num_blocks, BS, Hkv, 128]
   __half* v_cache;
+  // shared-prefix groups (grouped launches only; seq_group == nullptr otherwise)
+  const int32_t* seq_group;     // [S] group of each sequence
+  const int32_t* group_first;   // [num_groups + 1] first sequence of each group
+  const int32_t* group_shared;  // [num_groups] tokens the whole group shares
   int64_t num_blocks;
-  int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size;
+  int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   float scale_log2;
 };
 
 inline int tiles_for_tokens(int64_t tokens) { return static_cast<int>((tokens + kTile - 1) / kTile); }
 inline int max_splits_for(int max_blocks, int block_size) {
   const int tiles = tiles_for_tokens(static_cast<int64_t>(max_blocks) * block_size);
+  return (tiles + kPartitionTiles - 1) / kPartitionTiles;
+}
+
+// Tiles a sequence shares with its group (0 outside grouped launches) and the
+// split slots those take in the workspace.  The shared part always ends on a
+// tile boundary (the host checks group_shared % 16 == 0).
+__device__ __forceinline__ int shared_tiles_of(const Params& p, int s) {
+  return p.seq_group ? __ldg(p.group_shared + __ldg(p.seq_group + s)) / kTile : 0;
+}
+__device__ __forceinline__ int splits_for_tiles(int tiles) {
   return (tiles + kPartitionTiles - 1) / kPartitionTiles;
 }
 
@@ -170,82 +184,148 @@ __device__ __forceinline__ void process_tile(uint32_t st, const uint32_t (&qa)[8
   }
 }
 
-// Physical block ids of local tile j of a warp (second id only when BS == 8).
+
+__device__ __forceinline__ void mma_16816_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+      " {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// The same tile with all 16 MMA rows real (a shared-prefix group: one row per
+// (member sequence, query head)).  Every token of a shared tile is valid.
+// Lane holds rows r0 = lane / 4 and r1 = r0 + 8: m[0], l[0] and o[nd][0..1]
+// belong to r0; m[1], l[1] and o[nd][2..3] to r1.
+__device__ __forceinline__ void process_tile16(uint32_t st, const uint32_t (&qa)[8][4], int lane,
+                                               float scale_log2, float (&m)[2], float (&l)[2],
+                                               float (&o)[16][4]) {
+  constexpr unsigned kFull = 0xffffffffu;
+  const int r8 = lane & 7, mi = lane >> 3;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  const int ktok = r8 + ((mi >> 1) << 3);
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc) {
+    uint32_t b00, b01, b10, b11;
+    ldsm_x4(tile_chunk(st, 0, ktok, 2 * kc + (mi & 1)), b00, b01, b10, b11);
+    mma_16816_full(s0, qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b00, b01);
+    mma_16816_full(s1, qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b10, b11);
+  }
+  uint32_t pa[4];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float x0 = s0[2 * r] * scale_log2, x1 = s0[2 * r + 1] * scale_log2;
+    const float x2 = s1[2 * r] * scale_log2, x3 = s1[2 * r + 1] * scale_log2;
+    float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 1));
+    bm = fmaxf(bm, __shfl_xor_sync(kFull, bm, 2));
+    if (bm > m[r] + kRescaleThreshold) {
+      const float alpha = exp2_approx(m[r] - bm);
+      l[r] *= alpha;
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd) {
+        o[nd][2 * r] *= alpha;
+        o[nd][2 * r + 1] *= alpha;
+      }
+      m[r] = bm;
+    }
+    const float p0 = exp2_approx(x0 - m[r]), p1 = exp2_approx(x1 - m[r]);
+    const float p2 = exp2_approx(x2 - m[r]), p3 = exp2_approx(x3 - m[r]);
+    l[r] += (p0 + p1) + (p2 + p3);
+    pa[r] = pack_half2(p0, p1);       // a0 (row r0) / a1 (row r1): tokens 2(lane%4)..
+    pa[2 + r] = pack_half2(p2, p3);   // a2 / a3: tokens 8 + 2(lane%4)..
+  }
+  const int vtok = r8 + ((mi & 1) << 3);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t v0, v1, v2, v3;
+    ldsm_x4_trans(tile_chunk(st, 2, vtok, 2 * j + (mi >> 1)), v0, v1, v2, v3);
+    mma_16816_full(o[2 * j], pa[0], pa[1], pa[2], pa[3], v0, v1);
+    mma_16816_full(o[2 * j + 1], pa[0], pa[1], pa[2], pa[3], v2, v3);
+  }
+}
+
+// Physical block ids of one tile (second id only when BS == 8).
 struct TileIds {
   int32_t a, b;
 };
 
-template <int G, int BS, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
-    paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                 const __grid_constant__ CUtensorMap tmap_v, const Params p) {
-  static_assert(G >= 1 && G <= 8, "query rows of the MMA tile");
-  static_assert(BS == 8 || BS == 16 || BS == 32 || BS == 64, "block sizes with a kernel");
-  constexpr unsigned kFull = 0xffffffffu;
-  constexpr int kBlocksPerTile = BS < kTile ? kTile / BS : 1;  // 2 for BS = 8
-  constexpr int kBoxRows = BS < kTile ? BS : kTile;
-  constexpr uint32_t kBoxBytes = kBoxRows * 128;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+// The per-warp TMA pipeline over the tiles tile_begin + warp + 4 j of one
+// table row: lane j keeps the ids of the warp's j-th tile, lane 0 keeps
+// kStages tiles in flight, run() hands every landed tile to a callback.
+template <int BS>
+struct TileStream {
+  static constexpr unsigned kFull = 0xffffffffu;
+  static constexpr int kBlocksPerTile = BS < kTile ? kTile / BS : 1;  // 2 for BS = 8
+  static constexpr int kBoxRows = BS < kTile ? BS : kTile;
+  static constexpr uint32_t kBoxBytes = kBoxRows * 128;
 
-  const int g = blockIdx.x, s = blockIdx.y, split = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hq = p.num_q_heads;
-  const int h0 = g * G;
+  uint8_t* stages;        // this warp's ring
+  uint64_t* bars;
+  const CUtensorMap* tk;
+  const CUtensorMap* tv;
+  int warp, lane, g, tile_begin, my_count, issued;
+  TileIds my_ids;
 
-  const int L = clamp_context<BS>(p, s, threadIdx.x == 0 && g == 0 && split == 0);
-  const int ntiles = (L + kTile - 1) / kTile;
-  const int nsplit = (ntiles + kPartitionTiles - 1) / kPartitionTiles;
-  if (L == 0) {
-    if (split == 0) {
-      __half* o = p.out + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
-      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) o[i] = __float2half_rn(0.f);
-    }
-    return;
-  }
-  const int tile_begin = split * kPartitionTiles;
-  if (tile_begin >= ntiles) return;
-  const int n_here = min(kPartitionTiles, ntiles - tile_begin);
-  // warp w streams local tiles w, w + 4, ...; lane j holds the ids of its j-th
-  const int my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Smem::bars) + warp * kStages;
-  const uint32_t ring = smem_u32(smem + Smem::stages + warp * kStages * kStageBytes);
-
-  const int32_t* trow = p.block_tables + static_cast<int64_t>(s) * p.max_blocks;
-  TileIds my_ids = {-1, -1};
-  if (lane < my_count) {
-    const int tile = tile_begin + warp + lane * kWarps;
-    const int first_tok = tile * kTile;
+  // ids_limit: tokens at or past it have no block (the context length).
+  __device__ __forceinline__ void init(uint8_t* smem, const CUtensorMap* tk_, const CUtensorMap* tv_,
+                                       int g_, const int32_t* trow, int tile_begin_, int n_here,
+                                       int ids_limit, const Params& p) {
+    warp = threadIdx.x >> 5;
+    lane = threadIdx.x & 31;
+    tk = tk_;
+    tv = tv_;
+    g = g_;
+    tile_begin = tile_begin_;
+    my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
+    stages = smem + Smem::stages + warp * kStages * kStageBytes;
+    bars = reinterpret_cast<uint64_t*>(smem + Smem::bars) + warp * kStages;
+    my_ids.a = my_ids.b = -1;
+    if (lane < my_count) {
+      const int first_tok = (tile_begin + warp + lane * kWarps) * kTile;
 #pragma unroll
-    for (int q = 0; q < kBlocksPerTile; ++q) {
-      const int tok = first_tok + q * BS;
-      int32_t b = -1;
-      if (tok < L) {
-        b = __ldg(trow + tok / BS);
-        if (b < 0 || b >= p.num_blocks) {
-          report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
-          b = -2;  // poison the whole tile
+      for (int q = 0; q < kBlocksPerTile; ++q) {
+        const int tok = first_tok + q * BS;
+        int32_t b = -1;
+        if (tok < ids_limit) {
+          b = __ldg(trow + tok / BS);
+          if (b < 0 || b >= p.num_blocks) {
+            report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
+            b = -2;  // poison the whole tile
+          }
         }
+        if (q == 0) my_ids.a = b; else my_ids.b = b;
       }
-      if (q == 0) my_ids.a = b; else my_ids.b = b;
+      if (my_ids.b == -2) my_ids.a = -2;
     }
-    if (my_ids.b == -2) my_ids.a = -2;
-  }
-  if (lane == 0) {
-    if (warp == 0) {
-      prefetch_tmap(&tmap_k);
-      prefetch_tmap(&tmap_v);
+    if (lane == 0) {
+      if (warp == 0) {
+        prefetch_tmap(tk);
+        prefetch_tmap(tv);
+      }
+      for (int j = 0; j < kStages; ++j) mbar_init(&bars[j], 1);
+      fence_barrier_init();
     }
-    for (int j = 0; j < kStages; ++j) mbar_init(&bars[j], 1);
-    fence_barrier_init();
+    __syncwarp();
+    issued = min(kStages, my_count);
+#pragma unroll
+    for (int k = 0; k < kStages; ++k) {
+      const TileIds t = ids_of(k);
+      if (lane == 0 && k < issued) issue(k, t);
+    }
   }
-  __syncwarp();
+
+  __device__ __forceinline__ TileIds ids_of(int k) const {
+    TileIds t;
+    t.a = __shfl_sync(kFull, my_ids.a, k);
+    t.b = __shfl_sync(kFull, my_ids.b, k);
+    return t;
+  }
 
   // lane 0 only: local tile k with physical block(s) ids
-  auto issue = [&](int k, TileIds ids) {
+  __device__ __forceinline__ void issue(int k, TileIds ids) {
     uint64_t* bar = &bars[k % kStages];
-    uint8_t* st = smem + Smem::stages + (warp * kStages + k % kStages) * kStageBytes;
+    uint8_t* st = stages + (k % kStages) * kStageBytes;
     if (ids.a < 0) {  // reported already: complete the phase without data
       mbar_arrive(bar);
       return;
@@ -258,25 +338,103 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (q == 1 && nboxes == 1) break;
       const int row = (q == 0 ? ids.a : ids.b) * BS + row_in_block;
       const uint32_t off = q * kBoxBytes;
-      tma_load_3d(st + off, &tmap_k, 0, g, row, bar);
-      tma_load_3d(st + kHalfTileBytes + off, &tmap_k, 64, g, row, bar);
-      tma_load_3d(st + 2 * kHalfTileBytes + off, &tmap_v, 0, g, row, bar);
-      tma_load_3d(st + 3 * kHalfTileBytes + off, &tmap_v, 64, g, row, bar);
+      tma_load_3d(st + off, tk, 0, g, row, bar);
+      tma_load_3d(st + kHalfTileBytes + off, tk, 64, g, row, bar);
+      tma_load_3d(st + 2 * kHalfTileBytes + off, tv, 0, g, row, bar);
+      tma_load_3d(st + 3 * kHalfTileBytes + off, tv, 64, g, row, bar);
     }
-  };
-  auto ids_of = [&](int k) {
-    TileIds t;
-    t.a = __shfl_sync(kFull, my_ids.a, k);
-    t.b = __shfl_sync(kFull, my_ids.b, k);
-    return t;
-  };
-
-  int issued = min(kStages, my_count);
-#pragma unroll
-  for (int k = 0; k < kStages; ++k) {
-    const TileIds t = ids_of(k);
-    if (lane == 0 && k < issued) issue(k, t);
   }
+
+  // f(stage smem address, tile index, ids) for every tile that landed.
+  template <class F>
+  __device__ __forceinline__ void run(int32_t* dev_err, F&& f) {
+    bool ok = true;
+    for (int k = 0; k < issued; ++k) {
+      const int stage = k % kStages;
+      const bool landed = mbar_wait_bounded(&bars[stage], (k / kStages) & 1, dev_err);
+      ok = __all_sync(kFull, ok && landed) != 0;
+      const TileIds t = ids_of(k);
+      if (ok && t.a >= 0) f(smem_u32(stages + stage * kStageBytes), tile_begin + warp + k * kWarps, t);
+      __syncwarp();
+      const TileIds nt = ids_of(issued < 32 ? issued : 0);
+      if (ok && issued < my_count) {
+        if (lane == 0) issue(issued, nt);
+        ++issued;
+      }
+    }
+  }
+};
+
+// Combine the 4 warps' (m, l, o) of `rows` query rows held in shared memory
+// (ml [warps][16][2], ob [warps][16][128]) and hand each row's (M, den, num)
+// to emit(row, d, M, den, num) for every output dim d.
+template <class Emit>
+__device__ __forceinline__ void merge_warps(const float* ml, const float* ob, int rows, Emit&& emit) {
+  for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
+    const int r = e / kHeadDim, d = e % kHeadDim;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 16 + r) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float c = exp2_approx(ml[(w * 16 + r) * 2] - M);
+        num += c * ob[(w * 16 + r) * kHeadDim + d];
+        den += c * ml[(w * 16 + r) * 2 + 1];
+      }
+    }
+    emit(r, d, M, den, num);
+  }
+}
+
+__device__ __forceinline__ void store_partial(const Params& p, int64_t row, int slot, int d,
+                                              float M, float den, float num) {
+  const int64_t at = row * p.max_splits + slot;
+  p.part_o[at * kHeadDim + d] = num;
+  if (d == 0) {
+    p.part_ml[at * 2] = M;
+    p.part_ml[at * 2 + 1] = den;
+  }
+}
+
+// One CTA per (KV head, sequence, split of its own tiles).  In grouped launches
+// a sequence's own tiles start after the prefix its group shares, and its
+// partials go after the group's shared splits.
+template <int G, int BS, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                 const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  static_assert(G >= 1 && G <= 8, "query rows of the MMA tile");
+  static_assert(BS == 8 || BS == 16 || BS == 32 || BS == 64, "block sizes with a kernel");
+  constexpr unsigned kFull = 0xffffffffu;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+
+  const int g = blockIdx.x, s = blockIdx.y, split = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads;
+  const int h0 = g * G;
+
+  const int L = clamp_context<BS>(p, s, threadIdx.x == 0 && g == 0 && split == 0);
+  const int ntiles = (L + kTile - 1) / kTile;
+  const int own_begin = min(shared_tiles_of(p, s), ntiles);
+  const int shared_splits = splits_for_tiles(own_begin);
+  const int nsplit = shared_splits + splits_for_tiles(ntiles - own_begin);
+  if (L == 0) {
+    if (split == 0) {
+      __half* o = p.out + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
+      for (int i = threadIdx.x; i < G * kHeadDim; i += kThreads) o[i] = __float2half_rn(0.f);
+    }
+    return;
+  }
+  const int tile_begin = own_begin + split * kPartitionTiles;
+  if (tile_begin >= ntiles) return;
+  const int n_here = min(kPartitionTiles, ntiles - tile_begin);
+
+  TileStream<BS> ts;
+  ts.init(smem, &tmap_k, &tmap_v, g, p.block_tables + static_cast<int64_t>(s) * p.max_blocks,
+          tile_begin, n_here, L, p);
 
   // q of this lane's row as m16n8k16 A fragments (raw fp16; scale applied to S)
   uint32_t qa[8][2];
@@ -301,44 +459,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   float o[16][4];
 #pragma unroll
   for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
-  bool ok = true;
-  for (int k = 0; k < issued; ++k) {
-    const int stage = k % kStages;
-    const bool landed = mbar_wait_bounded(&bars[stage], (k / kStages) & 1, p.dev_err);
-    ok = __all_sync(kFull, ok && landed) != 0;
-    const TileIds t = ids_of(k);
-    const int tile = tile_begin + warp + k * kWarps;
-    if (ok && t.a >= 0) {
-      const uint32_t st = ring + stage * kStageBytes;
-      if (FUSED && tile == new_tile) {
-        // cache write of the new token: global slot and the staged row
-        const int32_t blk = (BS < kTile && new_row >= BS) ? t.b : t.a;
-        const int row_in_block = (L - 1) % BS;
-        const int c = lane & 15;
-        const bool is_v = lane >= 16;
-        const int64_t src = (static_cast<int64_t>(s) * p.num_kv_heads + g) * kHeadDim + c * 8;
-        const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
-        const int64_t dst =
-            ((static_cast<int64_t>(blk) * BS + row_in_block) * p.num_kv_heads + g) * kHeadDim +
-            c * 8;
-        *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) + dst) = val;
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         tile_chunk(st, is_v ? 2 : 0, new_row, c)),
-                     "r"(val.x), "r"(val.y), "r"(val.z), "r"(val.w)
-                     : "memory");
-        fence_proxy_async_smem();
-        __syncwarp();
-      }
-      const int valid = min(kTile, L - tile * kTile);
-      process_tile(st, qa, valid, lane, p.scale_log2, m, l, o);
+  ts.run(p.dev_err, [&](uint32_t st, int tile, TileIds t) {
+    if (FUSED && tile == new_tile) {
+      // cache write of the new token: global slot and the staged row
+      const int32_t blk = (BS < kTile && new_row >= BS) ? t.b : t.a;
+      const int row_in_block = (L - 1) % BS;
+      const int c = lane & 15;
+      const bool is_v = lane >= 16;
+      const int64_t src = (static_cast<int64_t>(s) * p.num_kv_heads + g) * kHeadDim + c * 8;
+      const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+      const int64_t dst =
+          ((static_cast<int64_t>(blk) * BS + row_in_block) * p.num_kv_heads + g) * kHeadDim +
+          c * 8;
+      *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) + dst) = val;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(
+                       tile_chunk(st, is_v ? 2 : 0, new_row, c)),
+                   "r"(val.x), "r"(val.y), "r"(val.z), "r"(val.w)
+                   : "memory");
+      fence_proxy_async_smem();
+      __syncwarp();
     }
-    __syncwarp();
-    const TileIds nt = ids_of(issued < 32 ? issued : 0);
-    if (ok && issued < my_count) {
-      if (lane == 0) issue(issued, nt);
-      ++issued;
-    }
-  }
+    process_tile(st, qa, min(kTile, L - tile * kTile), lane, p.scale_log2, m, l, o);
+  });
   l += __shfl_xor_sync(kFull, l, 1);
   l += __shfl_xor_sync(kFull, l, 2);
 
@@ -348,81 +490,200 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* ob = reinterpret_cast<float*>(smem + Smem::stages);
   if (qrow < G) {
     if ((lane & 3) == 0) {
-      ml[(warp * 8 + qrow) * 2] = m;
-      ml[(warp * 8 + qrow) * 2 + 1] = l;
+      ml[(warp * 16 + qrow) * 2] = m;
+      ml[(warp * 16 + qrow) * 2 + 1] = l;
     }
-    float* orow = ob + (warp * 8 + qrow) * kHeadDim + 2 * (lane & 3);
+    float* orow = ob + (warp * 16 + qrow) * kHeadDim + 2 * (lane & 3);
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd)
       *reinterpret_cast<float2*>(orow + nd * 8) = make_float2(o[nd][0], o[nd][1]);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
-    const int gi = e / kHeadDim, d = e % kHeadDim;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 8 + gi) * 2]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float c = exp2_approx(ml[(w * 8 + gi) * 2] - M);
-        num += c * ob[(w * 8 + gi) * kHeadDim + d];
-        den += c * ml[(w * 8 + gi) * 2 + 1];
-      }
-    }
+  merge_warps(ml, ob, G, [&](int gi, int d, float M, float den, float num) {
     const int64_t row = static_cast<int64_t>(s) * Hq + h0 + gi;
-    if (nsplit == 1) {
+    if (nsplit == 1)
       p.out[row * kHeadDim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
-    } else {
-      const int64_t slot = row * p.max_splits + split;
-      p.part_o[slot * kHeadDim + d] = num;
-      if (d == 0) {
-        p.part_ml[slot * 2] = M;
-        p.part_ml[slot * 2 + 1] = den;
-      }
+    else
+      store_partial(p, row, shared_splits + split, d, M, den, num);
+  });
+}
+
+// Shared prefix of a group: one CTA per (KV head, group, split of the shared
+// tiles) streams each shared tile once for every member, the members' query
+// heads being the 16 rows of the MMA tile (members x G <= 16).  It writes one
+// partial per member row into the group's first split slots; the members' own
+// tiles go through paged_attention_split_kernel and the merge kernel combines.
+template <int G, int BS>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_attention_shared_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  constexpr unsigned kFull = 0xffffffffu;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  const int g = blockIdx.x, grp = blockIdx.y, split = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hq = p.num_q_heads;
+
+  const int first = __ldg(p.group_first + grp);
+  const int members = __ldg(p.group_first + grp + 1) - first;
+  const int shared = __ldg(p.group_shared + grp);
+  const int rows = members * G;
+  if (shared <= 0 || members <= 0) return;
+  if (rows > 16 || shared % kTile != 0) {
+    if (threadIdx.x == 0 && g == 0 && split == 0) report(p.dev_err, PKV_DEV_BAD_GROUP);
+    return;
+  }
+  const int shared_tiles = shared / kTile;
+  const int tile_begin = split * kPartitionTiles;
+  if (tile_begin >= shared_tiles) return;
+  const int n_here = min(kPartitionTiles, shared_tiles - tile_begin);
+
+  // every member must hold the shared tokens through the leader's blocks
+  const int32_t* lead = p.block_tables + static_cast<int64_t>(first) * p.max_blocks;
+  {
+    const int blk_lo = tile_begin * kTile / BS;
+    const int blk_hi = (tile_begin + n_here) * kTile / BS;  // shared % BS == 0 (host check)
+    const int nblk = blk_hi - blk_lo;
+    for (int i = threadIdx.x; i < members * nblk; i += kThreads) {
+      const int mem = i / nblk, b = blk_lo + i % nblk;
+      const int32_t* row = p.block_tables + static_cast<int64_t>(first + mem) * p.max_blocks;
+      const int Lm = __ldg(p.context_lens + first + mem);
+      if (__ldg(row + b) != __ldg(lead + b) || Lm < shared) report(p.dev_err, PKV_DEV_BAD_GROUP);
     }
   }
+
+  TileStream<BS> ts;
+  ts.init(smem, &tmap_k, &tmap_v, g, lead, tile_begin, n_here, shared, p);
+
+  // A fragments of rows r0 = lane/4 and r1 = r0 + 8: row r is member r / G,
+  // query head g*G + r % G
+  uint32_t qa[8][4];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int r = (lane >> 2) + 8 * half;
+    if (r < rows) {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(
+          p.q + (static_cast<int64_t>(first + r / G) * Hq + g * G + r % G) * kHeadDim);
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        qa[kc][half] = __ldg(qp + 8 * kc + (lane & 3));
+        qa[kc][2 + half] = __ldg(qp + 8 * kc + 4 + (lane & 3));
+      }
+    } else {
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) qa[kc][half] = qa[kc][2 + half] = 0u;
+    }
+  }
+
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  float o[16][4];
+#pragma unroll
+  for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  ts.run(p.dev_err, [&](uint32_t st, int, TileIds) {
+    process_tile16(st, qa, lane, p.scale_log2, m, l, o);
+  });
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    l[r] += __shfl_xor_sync(kFull, l[r], 1);
+    l[r] += __shfl_xor_sync(kFull, l[r], 2);
+  }
+
+  __syncthreads();
+  float* ml = reinterpret_cast<float*>(smem + Smem::ml);
+  float* ob = reinterpret_cast<float*>(smem + Smem::stages);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int r = (lane >> 2) + 8 * half;
+    if (r < rows) {
+      if ((lane & 3) == 0) {
+        ml[(warp * 16 + r) * 2] = m[half];
+        ml[(warp * 16 + r) * 2 + 1] = l[half];
+      }
+      float* orow = ob + (warp * 16 + r) * kHeadDim + 2 * (lane & 3);
+#pragma unroll
+      for (int nd = 0; nd < 16; ++nd)
+        *reinterpret_cast<float2*>(orow + nd * 8) =
+            make_float2(o[nd][2 * half], o[nd][2 * half + 1]);
+    }
+  }
+  __syncthreads();
+  merge_warps(ml, ob, rows, [&](int r, int d, float M, float den, float num) {
+    const int64_t row = static_cast<int64_t>(first + r / G) * Hq + g * G + r % G;
+    store_partial(p, row, split, d, M, den, num);
+  });
 }
 
 // ---- host side: launch of one instantiation ---------------------------------------
-template <int G, int BS, bool FUSED>
-int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-               cudaStream_t stream) {
-  // The shared-memory opt-in is per device; remember it for up to 64 devices.
-  static std::atomic<uint8_t> opted_in[64];
+// The shared-memory opt-in is per kernel and per device; cudaFuncSetAttribute is
+// cheap but not free, so each kernel instantiation remembers it in its own
+// flags (one per device, up to 64).
+template <class Kernel>
+int opt_in_smem(Kernel kernel, std::atomic<uint8_t> (&opted_in)[64]) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
   if (dev < 0 || dev >= 64 || !opted_in[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(paged_attention_split_kernel<G, BS, FUSED>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem::alloc) != cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::alloc) !=
+        cudaSuccess)
       return PKV_ERR_CUDA;
     if (dev >= 0 && dev < 64) opted_in[dev].store(1, std::memory_order_release);
   }
-  dim3 grid(p.num_kv_heads, p.num_seqs, p.max_splits);
+  return PKV_OK;
+}
+
+template <int G, int BS, bool FUSED>
+int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, int private_splits,
+               cudaStream_t stream) {
+  static std::atomic<uint8_t> opted_in[64];
+  const int rc = opt_in_smem(paged_attention_split_kernel<G, BS, FUSED>, opted_in);
+  if (rc != PKV_OK) return rc;
+  dim3 grid(p.num_kv_heads, p.num_seqs, private_splits);
   paged_attention_split_kernel<G, BS, FUSED><<<grid, kThreads, Smem::alloc, stream>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-// Host launcher of the split kernel for one block size (attention_bs*.cu).
+template <int G, int BS>
+int launch_shared(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
+                  int shared_splits, cudaStream_t stream) {
+  static std::atomic<uint8_t> opted_in[64];
+  const int rc = opt_in_smem(paged_attention_shared_kernel<G, BS>, opted_in);
+  if (rc != PKV_OK) return rc;
+  dim3 grid(p.num_kv_heads, p.num_groups, shared_splits);
+  paged_attention_shared_kernel<G, BS><<<grid, kThreads, Smem::alloc, stream>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Host launchers for one block size (defined in attention_bs*.cu).
 template <int BS>
 int launch_split(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-                 cudaStream_t stream);
+                 int private_splits, cudaStream_t stream);
+template <int BS>
+int launch_shared_prefix(int G, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
+                         int shared_splits, cudaStream_t stream);
 
+#define PKV_CASE_G(GV, BSV)                                                                   \
+  case GV:                                                                                    \
+    return fused ? launch_one<GV, BSV, true>(mk, mv, p, ps, st)                               \
+                 : launch_one<GV, BSV, false>(mk, mv, p, ps, st);
 #define PKV_DEFINE_LAUNCH_SPLIT(BSV)                                                          \
   template <>                                                                                 \
   int launch_split<BSV>(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv,      \
-                        const Params& p, cudaStream_t st) {                                   \
+                        const Params& p, int ps, cudaStream_t st) {                           \
     switch (G) {                                                                              \
-      case 1: return fused ? launch_one<1, BSV, true>(mk, mv, p, st)                          \
-                           : launch_one<1, BSV, false>(mk, mv, p, st);                        \
-      case 2: return fused ? launch_one<2, BSV, true>(mk, mv, p, st)                          \
-                           : launch_one<2, BSV, false>(mk, mv, p, st);                        \
-      case 4: return fused ? launch_one<4, BSV, true>(mk, mv, p, st)                          \
-                           : launch_one<4, BSV, false>(mk, mv, p, st);                        \
-      case 8: return fused ? launch_one<8, BSV, true>(mk, mv, p, st)                          \
-                           : launch_one<8, BSV, false>(mk, mv, p, st);                        \
+      PKV_CASE_G(1, BSV)                                                                      \
+      PKV_CASE_G(2, BSV)                                                                      \
+      PKV_CASE_G(4, BSV)                                                                      \
+      PKV_CASE_G(8, BSV)                                                                      \
+      default: return PKV_ERR_UNSUPPORTED;                                                    \
+    }                                                                                         \
+  }                                                                                           \
+  template <>                                                                                 \
+  int launch_shared_prefix<BSV>(int G, const CUtensorMap& mk, const CUtensorMap& mv,          \
+                                const Params& p, int ss, cudaStream_t st) {                   \
+    switch (G) {                                                                              \
+      case 1: return launch_shared<1, BSV>(mk, mv, p, ss, st);                                \
+      case 2: return launch_shared<2, BSV>(mk, mv, p, ss, st);                                \
+      case 4: return launch_shared<4, BSV>(mk, mv, p, ss, st);                                \
+      case 8: return launch_shared<8, BSV>(mk, mv, p, ss, st);                                \
       default: return PKV_ERR_UNSUPPORTED;                                                    \
     }                                                                                         \
   }

@@ -13,15 +13,17 @@ namespace pkv {
 namespace attn {
 
 // Log-sum-exp merge of the splits of one (sequence, query head); 128 threads,
-// one output dim each.  Rows that needed a single split were written directly.
+// one output dim each.  Rows whose only split was written directly are skipped.
 __global__ void __launch_bounds__(kHeadDim) paged_attention_merge_kernel(const Params p) {
   const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
   int L = __ldg(p.context_lens + s);
   const int cap = p.max_blocks * p.block_size;
   L = L < 0 ? 0 : (L > cap ? cap : L);
   const int ntiles = (L + kTile - 1) / kTile;
-  const int nsplit = (ntiles + kPartitionTiles - 1) / kPartitionTiles;
-  if (nsplit <= 1) return;
+  const int own_begin = min(shared_tiles_of(p, s), ntiles);
+  const int shared_splits = splits_for_tiles(own_begin);
+  const int nsplit = shared_splits + splits_for_tiles(ntiles - own_begin);
+  if (nsplit == 0 || (nsplit == 1 && shared_splits == 0)) return;
   const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + h;
   const float* ml = p.part_ml + row * p.max_splits * 2;
   const float* po = p.part_o + row * p.max_splits * kHeadDim;
@@ -72,11 +74,20 @@ bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int64_
 bool supported_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 64; }
 
 // Shared validation + launch of both entry points.
+struct Groups {
+  const int32_t* first = nullptr;
+  const int32_t* seq_group = nullptr;
+  const int32_t* shared = nullptr;
+  int num_groups = 0;
+  int max_shared_tokens = 0;
+};
+
 int decode(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
            const void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
            int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
-           size_t workspace_bytes, int32_t* dev_err, void* stream, bool fused) {
+           size_t workspace_bytes, int32_t* dev_err, void* stream, bool fused,
+           const Groups& groups = Groups()) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -95,18 +106,34 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   if (num_blocks > INT32_MAX / block_size || num_seqs > 65535 || num_kv_heads > 65535)
     return PKV_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  const size_t need = pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
-                                                          max_blocks_per_seq, block_size,
-                                                          head_dim);
+  const bool grouped = groups.first != nullptr;
+  if (grouped) {
+    if (!groups.seq_group || !groups.shared || groups.num_groups <= 0 ||
+        groups.num_groups > 65535 || groups.max_shared_tokens < 0 || fused)
+      return PKV_ERR_INVALID_ARG;
+    if (groups.max_shared_tokens % kTile || groups.max_shared_tokens % block_size)
+      return PKV_ERR_INVALID_ARG;
+  }
+  const size_t need =
+      grouped ? pkv_paged_attention_grouped_workspace_bytes(num_seqs, num_q_heads,
+                                                            max_blocks_per_seq, block_size,
+                                                            head_dim, groups.max_shared_tokens)
+              : pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq,
+                                                    block_size, head_dim);
   if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return PKV_ERR_INVALID_ARG;
+  const int own_splits = max_splits_for(max_blocks_per_seq, block_size);
+  const int shared_splits =
+      grouped ? (tiles_for_tokens(groups.max_shared_tokens) + kPartitionTiles - 1) /
+                    kPartitionTiles
+              : 0;
 
   Params p;
   p.out = static_cast<__half*>(out);
   p.q = static_cast<const __half*>(q);
   p.block_tables = block_tables;
   p.context_lens = context_lens;
-  p.max_splits = max_splits_for(max_blocks_per_seq, block_size);
+  p.max_splits = own_splits + shared_splits;
   p.part_o = static_cast<float*>(workspace);
   p.part_ml = need ? p.part_o + static_cast<size_t>(num_seqs) * num_q_heads * p.max_splits *
                                     kHeadDim
@@ -122,6 +149,10 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.num_kv_heads = num_kv_heads;
   p.max_blocks = max_blocks_per_seq;
   p.block_size = block_size;
+  p.seq_group = grouped ? groups.seq_group : nullptr;
+  p.group_first = groups.first;
+  p.group_shared = groups.shared;
+  p.num_groups = groups.num_groups;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap mk, mv;
@@ -129,12 +160,21 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
       !make_cache_map(&mv, v_cache, num_kv_heads, num_blocks, block_size))
     return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc;
+  int rc = PKV_OK;
+  if (shared_splits > 0) {
+    switch (block_size) {
+      case 8: rc = launch_shared_prefix<8>(G, mk, mv, p, shared_splits, st); break;
+      case 16: rc = launch_shared_prefix<16>(G, mk, mv, p, shared_splits, st); break;
+      case 32: rc = launch_shared_prefix<32>(G, mk, mv, p, shared_splits, st); break;
+      default: rc = launch_shared_prefix<64>(G, mk, mv, p, shared_splits, st); break;
+    }
+    if (rc != PKV_OK) return rc;
+  }
   switch (block_size) {
-    case 8: rc = launch_split<8>(G, fused, mk, mv, p, st); break;
-    case 16: rc = launch_split<16>(G, fused, mk, mv, p, st); break;
-    case 32: rc = launch_split<32>(G, fused, mk, mv, p, st); break;
-    default: rc = launch_split<64>(G, fused, mk, mv, p, st); break;
+    case 8: rc = launch_split<8>(G, fused, mk, mv, p, own_splits, st); break;
+    case 16: rc = launch_split<16>(G, fused, mk, mv, p, own_splits, st); break;
+    case 32: rc = launch_split<32>(G, fused, mk, mv, p, own_splits, st); break;
+    default: rc = launch_split<64>(G, fused, mk, mv, p, own_splits, st); break;
   }
   if (rc != PKV_OK) return rc;
   if (p.max_splits > 1) {
@@ -157,6 +197,39 @@ extern "C" size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_he
   const int splits = max_splits_for(max_blocks_per_seq, block_size);
   if (splits <= 1) return 0;
   return static_cast<size_t>(num_seqs) * num_q_heads * splits * (kHeadDim + 2) * sizeof(float);
+}
+
+extern "C" size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads,
+                                                              int max_blocks_per_seq,
+                                                              int block_size, int head_dim,
+                                                              int max_shared_tokens) {
+  using namespace pkv::attn;
+  if (num_seqs <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || block_size <= 0 ||
+      head_dim != kHeadDim || max_shared_tokens < 0)
+    return 0;
+  const int splits = max_splits_for(max_blocks_per_seq, block_size) +
+                     (tiles_for_tokens(max_shared_tokens) + kPartitionTiles - 1) / kPartitionTiles;
+  return static_cast<size_t>(num_seqs) * num_q_heads * splits * (kHeadDim + 2) * sizeof(float);
+}
+
+extern "C" int pkv_paged_attention_decode_grouped(
+    void* out, const void* q, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* group_first,
+    const int32_t* seq_group, const int32_t* group_shared, int num_groups, int max_shared_tokens,
+    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  pkv::attn::Groups gr;
+  gr.first = group_first;
+  gr.seq_group = seq_group;
+  gr.shared = group_shared;
+  gr.num_groups = num_groups;
+  gr.max_shared_tokens = max_shared_tokens;
+  if (!group_first) return PKV_ERR_INVALID_ARG;
+  return pkv::attn::decode(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens,
+                           num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                           max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
+                           false, gr);
 }
 
 extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,

@@ -18,11 +18,14 @@ from .scenario import DecodeBatch
 
 class DecodeStep:
     def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None,
-                 fused=False):
+                 fused=False, grouped=False):
         """host_values: None draws q/K/V on the device (torch generator seeded by
         the workload); otherwise the tuple of ``workloads.host_tensors`` (numpy).
         fused: each layer is one launch of the fused cache-write + attention
-        kernel instead of reshape_and_cache followed by attention."""
+        kernel instead of reshape_and_cache followed by attention.
+        grouped: sequences sharing leading blocks (forked samples) are planned
+        into groups whose shared prefix is streamed once (reshape_and_cache
+        then grouped attention)."""
         self.fused = bool(fused)
         w = batch.workload
         self.batch = batch
@@ -52,7 +55,19 @@ class DecodeStep:
         self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(dev)
         self.cow_pairs = torch.from_numpy(batch.cow_pairs).to(dev)
         self.out = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
-        self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev, bs)
+        self.groups = None
+        if grouped:
+            gf, sg, gs, mx = ops.shared_prefix_groups(batch.block_tables, batch.context_lens, bs,
+                                                      16 // (Hq // Hkv))
+            if mx > 0:
+                self.groups = (torch.from_numpy(gf).to(dev), torch.from_numpy(sg).to(dev),
+                               torch.from_numpy(gs).to(dev), mx)
+                self.fused = False
+        if self.groups is not None:
+            n = ops.grouped_workspace_bytes(S, Hq, batch.max_blocks, self.groups[3], bs)
+            self.workspace = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
+        else:
+            self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev, bs)
         self.dev_err = ops.new_error_word(dev)
         self._host = None
 
@@ -74,6 +89,13 @@ class DecodeStep:
             return
         ops.reshape_and_cache(self.k_new[i], self.v_new[i], self.slot_mapping, self.k_cache[i],
                               self.v_cache[i], dev_err=self.dev_err, stream=stream)
+        if self.groups is not None:
+            gf, sg, gs, mx = self.groups
+            ops.paged_attention_decode_grouped(
+                self.out[i], self.q[i], self.k_cache[i], self.v_cache[i], self.block_tables,
+                self.context_lens, gf, sg, gs, mx, self.scale, workspace=self.workspace,
+                dev_err=self.dev_err, stream=stream)
+            return
         ops.paged_attention_decode(self.out[i], self.q[i], self.k_cache[i], self.v_cache[i],
                                    self.block_tables, self.context_lens, self.scale,
                                    workspace=self.workspace, dev_err=self.dev_err, stream=stream)
@@ -110,6 +132,8 @@ class DecodeStep:
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
                                          self.batch.max_blocks,
                                          self.batch.workload.block_size) else 0
+        if self.groups is not None:
+            return self.num_layers * 4      # cache write, shared prefix, own tiles, merge
         return self.num_layers * ((1 if self.fused else 2) + merge)
 
     def check_errors(self):

@@ -210,3 +210,79 @@ def swap_blocks(src_pools, dst_pools, block_pairs, dev_err=None, stream=None):
                                src_pools[0].shape[0], dst_pools[0].shape[0], _ptr(dev_err),
                                _stream_handle(stream))
     check(rc, "swap_blocks")
+
+
+def shared_prefix_groups(block_tables, context_lens, block_size=BLOCK_SIZE, group_size_limit=16):
+    """Host planning of grouped attention: consecutive sequences whose tables
+    start with the same physical blocks form a group (at most group_size_limit
+    members); a group shares the longest run of leading blocks every member
+    has in common with its first member, cut to a multiple of 16 tokens and of
+    the block size and to the shortest member's context.
+
+    Returns (group_first int32 [G+1], seq_group int32 [S], group_shared int32
+    [G], max_shared_tokens)."""
+    import numpy as np
+    tables = np.asarray(block_tables)
+    lens = np.asarray(context_lens)
+    S = len(lens)
+    unit = int(np.lcm(16, block_size))
+    first, shared, seq_group = [0], [], np.zeros(S, np.int32)
+    s = 0
+    while s < S:
+        e = s + 1
+        while (e < S and e - s < group_size_limit and lens[s] > 0 and lens[e] > 0
+               and tables[e, 0] == tables[s, 0]):
+            e += 1
+        tok = 0
+        if e - s > 1:
+            nb = min(-(-int(L) // block_size) for L in lens[s:e])
+            same = np.all(tables[s:e, :nb] == tables[s, :nb], axis=0)
+            lcp = nb if same.all() else int(np.argmin(same))
+            tok = min(lcp * block_size, int(lens[s:e].min()))
+            tok -= tok % unit
+        seq_group[s:e] = len(shared)
+        shared.append(tok)
+        first.append(e)
+        s = e
+    shared = np.array(shared, np.int32)
+    return (np.array(first, np.int32), seq_group, shared,
+            int(shared.max()) if len(shared) else 0)
+
+
+def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_shared_tokens,
+                            block_size=BLOCK_SIZE, head_dim=HEAD_DIM):
+    return int(lib().pkv_paged_attention_grouped_workspace_bytes(
+        num_seqs, num_q_heads, max_blocks_per_seq, block_size, head_dim, max_shared_tokens))
+
+
+def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   group_first, seq_group, group_shared, max_shared_tokens, scale,
+                                   workspace=None, dev_err=None, stream=None):
+    """Same result as paged_attention_decode; each group's shared prefix is read
+    once for all its members (see shared_prefix_groups)."""
+    _dev(q, "q", torch.float16, 3)
+    _dev(out, "out", torch.float16, 3)
+    _dev(k_cache, "k_cache", torch.float16, 4)
+    _dev(v_cache, "v_cache", torch.float16, 4)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    for name, t in (("group_first", group_first), ("seq_group", seq_group),
+                    ("group_shared", group_shared)):
+        _dev(t, name, torch.int32, 1)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    G = group_shared.shape[0]
+    if group_first.shape[0] != G + 1 or seq_group.shape[0] != S:
+        raise ValueError("group arrays do not match")
+    max_blocks = block_tables.shape[1]
+    need = grouped_workspace_bytes(S, Hq, max_blocks, int(max_shared_tokens), bs, D)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_decode_grouped(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(group_first), _ptr(seq_group), _ptr(group_shared), G, int(max_shared_tokens), S, Hq,
+        Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
+        _stream_handle(stream))
+    check(rc, "paged_attention_decode_grouped")
+    return out

@@ -1,0 +1,103 @@
+"""Grouped (shared-prefix) attention: the same result as plain paged attention,
+with each group's shared prefix streamed once for all its members."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import cache_ops as oc
+from parity_helpers import attention_tolerance, oracle_batch
+from paged_kv_cache_138_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+D = 128
+TOL = attention_tolerance()
+
+
+@pytest.fixture(scope="module")
+def ops(native_lib):
+    from paged_kv_cache_138_gb300 import ops as o
+    return o
+
+
+def forked_case(seed, groups, Hq, Hkv, bs, prefix_tokens, own_max=700):
+    """groups: members per group.  Each group's members share prefix_tokens of
+    blocks, then hold private blocks of 0..own_max further tokens."""
+    rng = np.random.default_rng(seed)
+    lens, rows = [], []
+    next_block = 0
+    pb = prefix_tokens // bs
+    for members in groups:
+        prefix = list(range(next_block, next_block + pb))
+        next_block += pb
+        for _ in range(members):
+            own = int(rng.integers(0, own_max + 1))
+            L = prefix_tokens + own
+            extra = -(-L // bs) - pb
+            rows.append(prefix + list(range(next_block, next_block + extra)))
+            next_block += extra
+            lens.append(L)
+    nb = next_block + 2
+    perm = rng.permutation(nb).astype(np.int32)        # scatter the blocks
+    mb = max(len(r) for r in rows)
+    tables = np.full((len(rows), mb), -1, np.int32)
+    for i, r in enumerate(rows):
+        tables[i, :len(r)] = perm[r]
+    q = wl.host_normal_fp16(rng, (len(rows), Hq, D))
+    kc = wl.host_normal_fp16(rng, (nb, bs, Hkv, D))
+    vc = wl.host_normal_fp16(rng, (nb, bs, Hkv, D))
+    return q, kc, vc, tables, np.array(lens, np.int32)
+
+
+def run_grouped(ops, q, kc, vc, tables, lens, bs, err=None):
+    gf, sg, gs, mx = ops.shared_prefix_groups(tables, lens, bs, 16 // (q.shape[1] // kc.shape[2]))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    e = ops.new_error_word() if err is None else err
+    ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
+                                       dev(gf), dev(sg), dev(gs), mx, 1 / np.sqrt(D), dev_err=e)
+    return out.cpu().numpy().astype(np.float64), ops.read_error_word(e), gs
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
+@pytest.mark.parametrize("Hq,Hkv,groups", [(8, 8, [16, 3, 1, 5]), (32, 8, [4, 4, 2, 1]),
+                                           (16, 8, [8, 1, 7])])
+@pytest.mark.parametrize("prefix", [512, 1024 + 512])
+def test_grouped_matches_oracle(ops, bs, Hq, Hkv, groups, prefix):
+    q, kc, vc, tables, lens = forked_case(bs + Hq + prefix, groups, Hq, Hkv, bs, prefix)
+    got, code, gs = run_grouped(ops, q, kc, vc, tables, lens, bs)
+    assert code == 0
+    assert (gs > 0).sum() == sum(1 for m in groups if m > 1)
+    ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= TOL
+
+
+def test_grouped_prefix_sharing_workload(ops):
+    """The prefix-sharing workload at full size (8 groups of 16 forked samples
+    sharing 2048 tokens), after its copy-on-write step."""
+    w = wl.WORKLOADS["prefix-sharing"]
+    tables, lens, slots, pairs, nb = oracle_batch(w)
+    q, k_new, v_new, kc, vc = wl.host_tensors(w, nb)
+    q, k_new, v_new, kc, vc = q[0], k_new[0], v_new[0], kc[0], vc[0]
+    oc.copy_blocks([kc], [vc], pairs)
+    oc.reshape_and_cache(k_new, v_new, slots, kc, vc)
+    got, code, gs = run_grouped(ops, q, kc, vc, tables, lens, 16)
+    assert code == 0 and list(gs) == [2048] * 8
+    ref = oa.paged_attention_decode(q, kc, vc, tables, lens, w.scale)
+    assert np.abs(got - ref).max() <= TOL
+
+
+def test_bad_group_is_reported(ops):
+    q, kc, vc, tables, lens = forked_case(3, [4], 8, 8, 16, 512)
+    gf = np.array([0, 4], np.int32)
+    sg = np.zeros(4, np.int32)
+    gs = np.array([512], np.int32)
+    tables = tables.copy()
+    tables[2, 3] = (tables[2, 3] + 1) % kc.shape[0]      # member 2 no longer shares block 3
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    err = ops.new_error_word()
+    ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
+                                       dev(gf), dev(sg), dev(gs), 512, 0.1, dev_err=err)
+    assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
