@@ -294,10 +294,10 @@ def run_ours(args):
                                           stream=stream)
                 attn_events[k][0].record(stream)
                 if step.groups is not None:
-                    gf, sg, gs, mx = step.groups
+                    gf, sg, gs, mx, mo = step.groups
                     ops.paged_attention_decode_grouped(
                         step.out[i], step.q[i], step.k_cache[i], step.v_cache[i],
-                        step.block_tables, step.context_lens, gf, sg, gs, mx, step.scale,
+                        step.block_tables, step.context_lens, gf, sg, gs, mx, mo, step.scale,
                         workspace=step.workspace, dev_err=step.dev_err, stream=stream)
                 elif step.fused:
                     ops.paged_attention_decode_fused(

@@ -166,14 +166,21 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
  *                 length, <= max_shared_tokens; 0 for no sharing.  Members x
  *                 (num_q_heads / num_kv_heads) must be <= 16.  Violations are
  *                 reported as PKV_DEV_BAD_GROUP.
+ *   max_own_tokens  the most tokens any sequence holds past its group's shared
+ *                 prefix (a sequence with group_shared 0 owns all its tokens);
+ *                 sizes the launch, and a sequence beyond it is reported as
+ *                 PKV_DEV_BAD_GROUP
  *   workspace     at least pkv_paged_attention_grouped_workspace_bytes(...)
- * The new tokens must already be in the cache (pkv_reshape_and_cache).
+ * The new tokens must already be in the cache (pkv_reshape_and_cache).  One
+ * kernel launch streams every shared prefix and every sequence's own tiles
+ * (the shared units first), a second merges the partials.
  */
 int pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_cache,
                                        const void* v_cache, const int32_t* block_tables,
                                        const int32_t* context_lens, const int32_t* group_first,
                                        const int32_t* seq_group, const int32_t* group_shared,
-                                       int num_groups, int max_shared_tokens, int num_seqs,
+                                       int num_groups, int max_shared_tokens,
+                                       int max_own_tokens, int num_seqs,
                                        int num_q_heads, int num_kv_heads, int head_dim,
                                        int block_size, int64_t num_blocks, int max_blocks_per_seq,
                                        float scale, void* workspace, size_t workspace_bytes,

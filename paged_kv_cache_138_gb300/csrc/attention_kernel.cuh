@@ -79,6 +79,7 @@ struct Params {
   const int32_t* group_shared;  // [num_groups] tokens the whole group shares
   int64_t num_blocks;
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
+  int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
   float scale_log2;
 };
 
@@ -402,16 +403,12 @@ __device__ __forceinline__ void store_partial(const Params& p, int64_t row, int 
 // a sequence's own tiles start after the prefix its group shares, and its
 // partials go after the group's shared splits.
 template <int G, int BS, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
-    paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                 const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+__device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                           const Params& p, uint8_t* smem, int g, int s,
+                                           int split) {
   static_assert(G >= 1 && G <= 8, "query rows of the MMA tile");
   static_assert(BS == 8 || BS == 16 || BS == 32 || BS == 64, "block sizes with a kernel");
   constexpr unsigned kFull = 0xffffffffu;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-
-  const int g = blockIdx.x, s = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads;
   const int h0 = g * G;
@@ -428,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     return;
   }
+  if (p.seq_group && split == 0 && threadIdx.x == 0 && ntiles - own_begin > p.own_tiles_cap)
+    report(p.dev_err, PKV_DEV_BAD_GROUP);  // more own tokens than the grid covers
   const int tile_begin = own_begin + split * kPartitionTiles;
   if (tile_begin >= ntiles) return;
   const int n_here = min(kPartitionTiles, ntiles - tile_begin);
@@ -514,13 +513,10 @@ __global__ void __launch_bounds__(kThreads, 2)
 // partial per member row into the group's first split slots; the members' own
 // tiles go through paged_attention_split_kernel and the merge kernel combines.
 template <int G, int BS>
-__global__ void __launch_bounds__(kThreads, 2)
-    paged_attention_shared_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+__device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                            const Params& p, uint8_t* smem, int g, int grp,
+                                            int split) {
   constexpr unsigned kFull = 0xffffffffu;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  const int g = blockIdx.x, grp = blockIdx.y, split = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = p.num_q_heads;
 
@@ -613,6 +609,43 @@ __global__ void __launch_bounds__(kThreads, 2)
   });
 }
 
+__device__ __forceinline__ uint8_t* aligned_smem() {
+  extern __shared__ uint8_t smem_raw[];
+  return smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+}
+
+// grid (KV heads, sequences, splits)
+template <int G, int BS, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                 const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  split_body<G, BS, FUSED>(tmap_k, tmap_v, p, aligned_smem(), blockIdx.x, blockIdx.y,
+                           blockIdx.z);
+}
+
+// One launch for a grouped step, 1-D grid: first the shared-prefix units
+// (KV head, group, shared split) -- the long ones, scheduled first -- then the
+// members' own units (KV head, sequence, own split).
+template <int G, int BS>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_attention_grouped_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                                   const __grid_constant__ CUtensorMap tmap_v, const Params p,
+                                   int shared_splits, int own_splits) {
+  uint8_t* smem = aligned_smem();
+  int u = blockIdx.x;
+  const int n_shared = p.num_kv_heads * p.num_groups * shared_splits;
+  if (u < n_shared) {
+    const int g = u % p.num_kv_heads;
+    u /= p.num_kv_heads;
+    shared_body<G, BS>(tmap_k, tmap_v, p, smem, g, u % p.num_groups, u / p.num_groups);
+  } else {
+    u -= n_shared;
+    const int g = u % p.num_kv_heads;
+    u /= p.num_kv_heads;
+    split_body<G, BS, false>(tmap_k, tmap_v, p, smem, g, u % p.num_seqs, u / p.num_seqs);
+  }
+}
+
 // ---- host side: launch of one instantiation ---------------------------------------
 // The shared-memory opt-in is per kernel and per device; cudaFuncSetAttribute is
 // cheap but not free, so each kernel instantiation remembers it in its own
@@ -642,13 +675,18 @@ int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, in
 }
 
 template <int G, int BS>
-int launch_shared(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-                  int shared_splits, cudaStream_t stream) {
+int launch_grouped(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
+                   int shared_splits, int own_splits, cudaStream_t stream) {
   static std::atomic<uint8_t> opted_in[64];
-  const int rc = opt_in_smem(paged_attention_shared_kernel<G, BS>, opted_in);
+  const int rc = opt_in_smem(paged_attention_grouped_kernel<G, BS>, opted_in);
   if (rc != PKV_OK) return rc;
-  dim3 grid(p.num_kv_heads, p.num_groups, shared_splits);
-  paged_attention_shared_kernel<G, BS><<<grid, kThreads, Smem::alloc, stream>>>(mk, mv, p);
+  const int64_t units = static_cast<int64_t>(p.num_kv_heads) *
+                        (static_cast<int64_t>(p.num_groups) * shared_splits +
+                         static_cast<int64_t>(p.num_seqs) * own_splits);
+  if (units <= 0) return PKV_OK;
+  if (units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  paged_attention_grouped_kernel<G, BS><<<static_cast<unsigned>(units), kThreads, Smem::alloc,
+                                          stream>>>(mk, mv, p, shared_splits, own_splits);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -657,8 +695,8 @@ template <int BS>
 int launch_split(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
                  int private_splits, cudaStream_t stream);
 template <int BS>
-int launch_shared_prefix(int G, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-                         int shared_splits, cudaStream_t stream);
+int launch_grouped_step(int G, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
+                        int shared_splits, int own_splits, cudaStream_t stream);
 
 #define PKV_CASE_G(GV, BSV)                                                                   \
   case GV:                                                                                    \
@@ -677,13 +715,13 @@ int launch_shared_prefix(int G, const CUtensorMap& mk, const CUtensorMap& mv, co
     }                                                                                         \
   }                                                                                           \
   template <>                                                                                 \
-  int launch_shared_prefix<BSV>(int G, const CUtensorMap& mk, const CUtensorMap& mv,          \
-                                const Params& p, int ss, cudaStream_t st) {                   \
+  int launch_grouped_step<BSV>(int G, const CUtensorMap& mk, const CUtensorMap& mv,           \
+                               const Params& p, int ss, int os, cudaStream_t st) {            \
     switch (G) {                                                                              \
-      case 1: return launch_shared<1, BSV>(mk, mv, p, ss, st);                                \
-      case 2: return launch_shared<2, BSV>(mk, mv, p, ss, st);                                \
-      case 4: return launch_shared<4, BSV>(mk, mv, p, ss, st);                                \
-      case 8: return launch_shared<8, BSV>(mk, mv, p, ss, st);                                \
+      case 1: return launch_grouped<1, BSV>(mk, mv, p, ss, os, st);                           \
+      case 2: return launch_grouped<2, BSV>(mk, mv, p, ss, os, st);                           \
+      case 4: return launch_grouped<4, BSV>(mk, mv, p, ss, os, st);                           \
+      case 8: return launch_grouped<8, BSV>(mk, mv, p, ss, os, st);                           \
       default: return PKV_ERR_UNSUPPORTED;                                                    \
     }                                                                                         \
   }

@@ -80,6 +80,7 @@ struct Groups {
   const int32_t* shared = nullptr;
   int num_groups = 0;
   int max_shared_tokens = 0;
+  int max_own_tokens = 0;  // longest stretch past a group's shared prefix
 };
 
 int decode(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
@@ -109,7 +110,8 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   const bool grouped = groups.first != nullptr;
   if (grouped) {
     if (!groups.seq_group || !groups.shared || groups.num_groups <= 0 ||
-        groups.num_groups > 65535 || groups.max_shared_tokens < 0 || fused)
+        groups.num_groups > 65535 || groups.max_shared_tokens < 0 ||
+        groups.max_own_tokens < 0 || fused)
       return PKV_ERR_INVALID_ARG;
     if (groups.max_shared_tokens % kTile || groups.max_shared_tokens % block_size)
       return PKV_ERR_INVALID_ARG;
@@ -153,6 +155,8 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.group_first = groups.first;
   p.group_shared = groups.shared;
   p.num_groups = groups.num_groups;
+  p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
+                    kPartitionTiles * kPartitionTiles;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap mk, mv;
@@ -161,20 +165,24 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
     return PKV_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc = PKV_OK;
-  if (shared_splits > 0) {
+  if (grouped) {
+    // own units: sequences never run past max_own_tokens beyond their shared
+    // prefix (a sequence outside any group counts all its tokens as its own)
+    const int own = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
+                    kPartitionTiles;
     switch (block_size) {
-      case 8: rc = launch_shared_prefix<8>(G, mk, mv, p, shared_splits, st); break;
-      case 16: rc = launch_shared_prefix<16>(G, mk, mv, p, shared_splits, st); break;
-      case 32: rc = launch_shared_prefix<32>(G, mk, mv, p, shared_splits, st); break;
-      default: rc = launch_shared_prefix<64>(G, mk, mv, p, shared_splits, st); break;
+      case 8: rc = launch_grouped_step<8>(G, mk, mv, p, shared_splits, own, st); break;
+      case 16: rc = launch_grouped_step<16>(G, mk, mv, p, shared_splits, own, st); break;
+      case 32: rc = launch_grouped_step<32>(G, mk, mv, p, shared_splits, own, st); break;
+      default: rc = launch_grouped_step<64>(G, mk, mv, p, shared_splits, own, st); break;
     }
-    if (rc != PKV_OK) return rc;
-  }
-  switch (block_size) {
-    case 8: rc = launch_split<8>(G, fused, mk, mv, p, own_splits, st); break;
-    case 16: rc = launch_split<16>(G, fused, mk, mv, p, own_splits, st); break;
-    case 32: rc = launch_split<32>(G, fused, mk, mv, p, own_splits, st); break;
-    default: rc = launch_split<64>(G, fused, mk, mv, p, own_splits, st); break;
+  } else {
+    switch (block_size) {
+      case 8: rc = launch_split<8>(G, fused, mk, mv, p, own_splits, st); break;
+      case 16: rc = launch_split<16>(G, fused, mk, mv, p, own_splits, st); break;
+      case 32: rc = launch_split<32>(G, fused, mk, mv, p, own_splits, st); break;
+      default: rc = launch_split<64>(G, fused, mk, mv, p, own_splits, st); break;
+    }
   }
   if (rc != PKV_OK) return rc;
   if (p.max_splits > 1) {
@@ -216,7 +224,7 @@ extern "C" int pkv_paged_attention_decode_grouped(
     void* out, const void* q, const void* k_cache, const void* v_cache,
     const int32_t* block_tables, const int32_t* context_lens, const int32_t* group_first,
     const int32_t* seq_group, const int32_t* group_shared, int num_groups, int max_shared_tokens,
-    int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_own_tokens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
     int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
     size_t workspace_bytes, int32_t* dev_err, void* stream) {
   pkv::attn::Groups gr;
@@ -225,6 +233,7 @@ extern "C" int pkv_paged_attention_decode_grouped(
   gr.shared = group_shared;
   gr.num_groups = num_groups;
   gr.max_shared_tokens = max_shared_tokens;
+  gr.max_own_tokens = max_own_tokens;
   if (!group_first) return PKV_ERR_INVALID_ARG;
   return pkv::attn::decode(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, context_lens,
                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,

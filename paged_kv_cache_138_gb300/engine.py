@@ -57,11 +57,11 @@ class DecodeStep:
         self.out = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
         self.groups = None
         if grouped:
-            gf, sg, gs, mx = ops.shared_prefix_groups(batch.block_tables, batch.context_lens, bs,
-                                                      16 // (Hq // Hkv))
+            gf, sg, gs, mx, mo = ops.shared_prefix_groups(batch.block_tables, batch.context_lens,
+                                                          bs, 16 // (Hq // Hkv))
             if mx > 0:
                 self.groups = (torch.from_numpy(gf).to(dev), torch.from_numpy(sg).to(dev),
-                               torch.from_numpy(gs).to(dev), mx)
+                               torch.from_numpy(gs).to(dev), mx, mo)
                 self.fused = False
         if self.groups is not None:
             n = ops.grouped_workspace_bytes(S, Hq, batch.max_blocks, self.groups[3], bs)
@@ -90,10 +90,10 @@ class DecodeStep:
         ops.reshape_and_cache(self.k_new[i], self.v_new[i], self.slot_mapping, self.k_cache[i],
                               self.v_cache[i], dev_err=self.dev_err, stream=stream)
         if self.groups is not None:
-            gf, sg, gs, mx = self.groups
+            gf, sg, gs, mx, mo = self.groups
             ops.paged_attention_decode_grouped(
                 self.out[i], self.q[i], self.k_cache[i], self.v_cache[i], self.block_tables,
-                self.context_lens, gf, sg, gs, mx, self.scale, workspace=self.workspace,
+                self.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
                 dev_err=self.dev_err, stream=stream)
             return
         ops.paged_attention_decode(self.out[i], self.q[i], self.k_cache[i], self.v_cache[i],
@@ -133,7 +133,7 @@ class DecodeStep:
                                          self.batch.max_blocks,
                                          self.batch.workload.block_size) else 0
         if self.groups is not None:
-            return self.num_layers * 4      # cache write, shared prefix, own tiles, merge
+            return self.num_layers * 3      # cache write, shared + own tiles, merge
         return self.num_layers * ((1 if self.fused else 2) + merge)
 
     def check_errors(self):

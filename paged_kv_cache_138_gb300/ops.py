@@ -220,7 +220,7 @@ def shared_prefix_groups(block_tables, context_lens, block_size=BLOCK_SIZE, grou
     the block size and to the shortest member's context.
 
     Returns (group_first int32 [G+1], seq_group int32 [S], group_shared int32
-    [G], max_shared_tokens)."""
+    [G], max_shared_tokens, max_own_tokens)."""
     import numpy as np
     tables = np.asarray(block_tables)
     lens = np.asarray(context_lens)
@@ -245,8 +245,9 @@ def shared_prefix_groups(block_tables, context_lens, block_size=BLOCK_SIZE, grou
         first.append(e)
         s = e
     shared = np.array(shared, np.int32)
+    own = lens.astype(np.int64) - shared[seq_group] if S else np.zeros(0, np.int64)
     return (np.array(first, np.int32), seq_group, shared,
-            int(shared.max()) if len(shared) else 0)
+            int(shared.max()) if len(shared) else 0, int(own.max()) if S else 0)
 
 
 def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_shared_tokens,
@@ -256,8 +257,9 @@ def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_share
 
 
 def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens,
-                                   group_first, seq_group, group_shared, max_shared_tokens, scale,
-                                   workspace=None, dev_err=None, stream=None):
+                                   group_first, seq_group, group_shared, max_shared_tokens,
+                                   max_own_tokens, scale, workspace=None, dev_err=None,
+                                   stream=None):
     """Same result as paged_attention_decode; each group's shared prefix is read
     once for all its members (see shared_prefix_groups)."""
     _dev(q, "q", torch.float16, 3)
@@ -281,7 +283,8 @@ def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, conte
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = lib().pkv_paged_attention_decode_grouped(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        _ptr(group_first), _ptr(seq_group), _ptr(group_shared), G, int(max_shared_tokens), S, Hq,
+        _ptr(group_first), _ptr(seq_group), _ptr(group_shared), G, int(max_shared_tokens),
+        int(max_own_tokens), S, Hq,
         Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
         _stream_handle(stream))
     check(rc, "paged_attention_decode_grouped")

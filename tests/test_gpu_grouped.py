@@ -50,12 +50,14 @@ def forked_case(seed, groups, Hq, Hkv, bs, prefix_tokens, own_max=700):
 
 
 def run_grouped(ops, q, kc, vc, tables, lens, bs, err=None):
-    gf, sg, gs, mx = ops.shared_prefix_groups(tables, lens, bs, 16 // (q.shape[1] // kc.shape[2]))
+    gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, bs,
+                                                  16 // (q.shape[1] // kc.shape[2]))
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
     e = ops.new_error_word() if err is None else err
     ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
-                                       dev(gf), dev(sg), dev(gs), mx, 1 / np.sqrt(D), dev_err=e)
+                                       dev(gf), dev(sg), dev(gs), mx, mo, 1 / np.sqrt(D),
+                                       dev_err=e)
     return out.cpu().numpy().astype(np.float64), ops.read_error_word(e), gs
 
 
@@ -99,5 +101,17 @@ def test_bad_group_is_reported(ops):
     out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
     err = ops.new_error_word()
     ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
-                                       dev(gf), dev(sg), dev(gs), 512, 0.1, dev_err=err)
+                                       dev(gf), dev(sg), dev(gs), 512, 700, 0.1, dev_err=err)
+    assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
+
+
+def test_own_tokens_beyond_the_stated_bound_are_reported(ops):
+    q, kc, vc, tables, lens = forked_case(4, [3, 2], 8, 8, 16, 512, own_max=900)
+    gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, 16, 16)
+    assert mo > 600
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    err = ops.new_error_word()
+    ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
+                                       dev(gf), dev(sg), dev(gs), mx, 100, 0.1, dev_err=err)
     assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
