@@ -454,12 +454,17 @@ def run_serving(args):
     reqs = wl.serving_requests(2024, num_requests=4096, num_system_prompts=4,
                                system_prompt_len=1024, suffix_max=512, new_min=64, new_max=512)
     nb = 64 * 110
+    grouped = args.grouped != "off"
     drv = ContinuousBatchDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
-                                sources=DeviceSources(7, Hq, Hkv), device=device)
+                                sources=DeviceSources(7, Hq, Hkv), device=device,
+                                grouped=grouped)
     for r in reqs:
         drv.add_request(r.rid, r.prompt, r.max_new_tokens)
+    import gc
+    gc.collect()
+    gc.freeze()     # the trace's token lists are long-lived: keep them out of GC scans
     stats = {"seq_steps": 0, "kv_tokens": 0, "preempted": 0, "admitted": 0, "cached": 0,
-             "prefill": 0}
+             "prefill": 0, "shared_tokens": 0}
     for _ in range(max(args.warmup, 3) * 20):
         drv.step()
     torch.cuda.synchronize(device)
@@ -475,6 +480,7 @@ def run_serving(args):
         stats["admitted"] += len(res.admitted)
         stats["cached"] += res.cached_tokens
         stats["prefill"] += res.prefill_tokens
+        stats["shared_tokens"] += res.shared_tokens
     e1.record()
     torch.cuda.synchronize(device)
     wall = time.perf_counter() - t0
@@ -484,8 +490,10 @@ def run_serving(args):
             "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f16 (fp32 accumulate)", "data": "synthetic",
-            "config": {"workload": "serving", "description": run_serving.__doc__.split(".")[0],
-                       "max_batch": 64, "pool_blocks": nb, "heads": Hq},
+            "config": {"workload": "serving", "description": " ".join(
+                run_serving.__doc__.split(".")[0].split()),
+                       "max_batch": 64, "pool_blocks": nb, "heads": Hq,
+                       "grouped_shared_prefix": grouped},
             "seq_steps_per_s": stats["seq_steps"] / wall,
             "device_ms_per_step": e0.elapsed_time(e1) / steps, "stats": stats}
     print(json.dumps(line))

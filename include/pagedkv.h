@@ -191,6 +191,25 @@ size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads
                                                    int max_blocks_per_seq, int block_size,
                                                    int head_dim, int max_shared_tokens);
 
+/*
+ * Host planning for pkv_paged_attention_decode_grouped (host memory only).
+ * Consecutive sequences whose tables start with the same physical block form a
+ * group of at most max_members (16 / (num_q_heads / num_kv_heads) for the
+ * kernel); a group shares the longest run of leading blocks that every member
+ * has in common with its first member, cut to a multiple of 16 tokens and of
+ * block_size and to the shortest member's context length.  Sequences are not
+ * reordered: sort them by their first block beforehand to group them all.
+ *   tables [num_seqs, max_blocks], context_lens [num_seqs] (host)
+ *   outputs (host): group_first [num_seqs + 1], seq_group [num_seqs],
+ *   group_shared [num_seqs] (the first *num_groups entries are used),
+ *   *max_shared_tokens, *max_own_tokens for the attention call.
+ */
+int pkv_plan_shared_prefix_groups(const int32_t* tables, const int32_t* context_lens,
+                                  int num_seqs, int max_blocks, int block_size, int max_members,
+                                  int32_t* group_first, int32_t* seq_group,
+                                  int32_t* group_shared, int* num_groups,
+                                  int* max_shared_tokens, int* max_own_tokens);
+
 /* ---- cache write --------------------------------------------------------- */
 /*
  * reshape_and_cache: store the K/V of new tokens at their slots.

@@ -72,6 +72,18 @@ class BlockManager:
         self._check(rc, "append_slots (%d done)" % done.value)
         return slots
 
+    def append_slots_partial(self, seqs, tokens):
+        """Like append_slots, but stops at the first failure instead of raising:
+        returns (slots int64 [n], number appended, status of the failing append
+        or PKV_OK)."""
+        seqs = np.ascontiguousarray(seqs, dtype=np.int64)
+        toks = _i32(tokens)
+        slots = np.empty(len(seqs), dtype=np.int64)
+        done = ctypes.c_int64()
+        rc = lib().pkv_bm_append_slots(self._h, _p(seqs), _p(toks), len(seqs), _p(slots),
+                                       ctypes.byref(done))
+        return slots, int(done.value), int(rc)
+
     def fork(self, parent, child):
         self._check(lib().pkv_bm_fork(self._h, int(parent), int(child)), "fork")
 

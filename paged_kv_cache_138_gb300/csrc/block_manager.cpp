@@ -5,6 +5,7 @@
 //
 // Every operation that can fail checks first and mutates afterwards, so a
 // PKV_ERR_OUT_OF_BLOCKS return leaves the manager exactly as it was.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <deque>
@@ -440,3 +441,61 @@ int pkv_bm_check_invariants(const pkv_block_manager* bm) {
 }
 
 }  // extern "C"
+
+// ---- shared-prefix group planning (host) -----------------------------------------
+// Consecutive sequences whose tables start with the same physical block form a
+// group of at most max_members; the group shares the longest run of leading
+// blocks every member has in common with its first member, cut to a multiple
+// of lcm(16, block_size) tokens and to the shortest member's context.
+extern "C" int pkv_plan_shared_prefix_groups(const int32_t* tables, const int32_t* context_lens,
+                                             int num_seqs, int max_blocks, int block_size,
+                                             int max_members, int32_t* group_first,
+                                             int32_t* seq_group, int32_t* group_shared,
+                                             int* num_groups, int* max_shared_tokens,
+                                             int* max_own_tokens) {
+  if (num_seqs < 0 || max_blocks <= 0 || block_size <= 0 || max_members <= 0 || !num_groups ||
+      !max_shared_tokens || !max_own_tokens)
+    return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!tables || !context_lens || !group_first || !seq_group || !group_shared))
+    return PKV_ERR_INVALID_ARG;
+  int64_t unit = 16;
+  while (unit % block_size) unit += 16;  // lcm(16, block_size) for the sizes in use
+  int groups = 0, max_shared = 0, max_own = 0;
+  int s = 0;
+  while (s < num_seqs) {
+    const int32_t* lead = tables + static_cast<int64_t>(s) * max_blocks;
+    int e = s + 1;
+    while (e < num_seqs && e - s < max_members && context_lens[s] > 0 && context_lens[e] > 0 &&
+           tables[static_cast<int64_t>(e) * max_blocks] == lead[0])
+      ++e;
+    int64_t shared = 0;
+    if (e - s > 1) {
+      int64_t min_len = context_lens[s];
+      for (int m = s + 1; m < e; ++m) min_len = std::min<int64_t>(min_len, context_lens[m]);
+      int64_t lcp = (min_len + block_size - 1) / block_size;
+      lcp = std::min<int64_t>(lcp, max_blocks);
+      for (int m = s + 1; m < e; ++m) {
+        const int32_t* row = tables + static_cast<int64_t>(m) * max_blocks;
+        int64_t k = 0;
+        while (k < lcp && row[k] == lead[k]) ++k;
+        lcp = k;
+      }
+      shared = std::min<int64_t>(lcp * block_size, min_len);
+      shared -= shared % unit;
+    }
+    group_first[groups] = s;
+    group_shared[groups] = static_cast<int32_t>(shared);
+    for (int m = s; m < e; ++m) {
+      seq_group[m] = groups;
+      max_own = std::max<int>(max_own, static_cast<int>(context_lens[m] - shared));
+    }
+    max_shared = std::max<int>(max_shared, static_cast<int>(shared));
+    ++groups;
+    s = e;
+  }
+  group_first[groups] = num_seqs;
+  *num_groups = groups;
+  *max_shared_tokens = max_shared;
+  *max_own_tokens = max_own;
+  return PKV_OK;
+}

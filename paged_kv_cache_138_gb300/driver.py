@@ -63,12 +63,15 @@ class StepResult:
     prefill_tokens: int = 0
     cached_tokens: int = 0
     kv_tokens: int = 0             # tokens attended over this step
+    groups: int = 0                # grouped launches: groups planned this step
+    shared_tokens: int = 0         # tokens read through a group's shared prefix
 
 
 class ContinuousBatchDriver:
     def __init__(self, num_blocks, num_q_heads, num_kv_heads, max_batch, max_blocks_per_seq,
                  sources, device="cuda", block_size=16, head_dim=128, enable_prefix_cache=True,
-                 free_order=None, record_ops=False, preemption="recompute", host_blocks=0):
+                 free_order=None, record_ops=False, preemption="recompute", host_blocks=0,
+                 grouped=False):
         """sources: object with
              next_token(req) -> int
              kv(req, positions) -> (k, v) fp16 CUDA tensors [n, Hkv, D] for the
@@ -98,6 +101,10 @@ class ContinuousBatchDriver:
         if preemption not in ("recompute", "swap"):
             raise ValueError("preemption is 'recompute' or 'swap'")
         self.preemption = preemption
+        # grouped attention: requests whose tables start with the same blocks
+        # (prefix-cache hits on a shared prompt) stream those blocks once
+        self.grouped = bool(grouped)
+        self.gws = None
         # swap space: pinned host pools for K and V and a FIFO of their free blocks
         self.host_k = self.host_v = None
         self.host_free = deque(range(host_blocks))
@@ -130,19 +137,32 @@ class ContinuousBatchDriver:
             self.ops_log.append(entry)
 
     # ---- device writes -------------------------------------------------------------
+    def _to_device(self, arr):
+        """Host array -> device through a pinned staging tensor (asynchronous)."""
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+        if self.dev.type == "cuda":
+            t = t.pin_memory()
+        return t.to(self.dev, non_blocking=True)
+
     def _write_kv(self, k, v, slots):
-        slot_t = torch.as_tensor(np.asarray(slots, dtype=np.int64)).to(self.dev, non_blocking=True)
+        slot_t = self._to_device(np.asarray(slots, dtype=np.int64))
         ops.reshape_and_cache(k, v, slot_t, self.k_cache, self.v_cache, dev_err=self.dev_err)
 
     def _prefill(self, req, cached):
         n = len(req.tokens)
         if cached >= n:
             return 0
-        positions = list(range(cached, n))
-        slots = [self.bm.slot(req.rid, p) for p in positions]
-        k, v = self.src.kv(req, positions)
+        positions = np.arange(cached, n)
+        table = np.asarray(self.bm.block_table(req.rid), dtype=np.int64)
+        slots = table[positions // self.bs] * self.bs + positions % self.bs
+        k, v = self.src.kv(req, positions.tolist())
         self._write_kv(k, v, slots)
         return len(positions)
+
+    def _next_tokens(self, reqs):
+        if hasattr(self.src, "next_tokens"):
+            return [int(t) for t in self.src.next_tokens(reqs)]
+        return [int(self.src.next_token(r)) for r in reqs]
 
     def _swap(self, pairs, out):
         pairs_d = torch.tensor(pairs, dtype=torch.int64, device=self.dev)
@@ -216,30 +236,39 @@ class ContinuousBatchDriver:
             res.cached_tokens += cached
             self.running.append(r)
             res.admitted.append(r.rid)
-        # 3. one decode token per running request
+        # 3. one decode token per running request: one native call appends for the
+        # whole batch; an OutOfBlocks stops it at the failing request, which is
+        # handled (preemption) before the call resumes from there
         batch, slots = [], []
-        for r in list(self.running):
-            if r not in self.running:       # preempted while serving an earlier request
-                continue
+        pending = list(self.running)
+        for r in pending:
             if len(r.tokens) + 1 > self.max_blocks * self.bs:
                 raise ValueError("request %d outgrew max_blocks_per_seq" % r.rid)
-            tok = self.src.next_token(r)
-            while True:
-                try:
-                    slot = self.bm.append_slot(r.rid, tok)
-                    self._log("append", r.rid, tok, slot)
-                    break
-                except OutOfBlocks:
-                    self._log("append", r.rid, tok, None)
-                    if self._preempt(res, batch) is r:
-                        slot = None
-                        break
-            if slot is None:
-                continue
-            r.tokens.append(tok)
-            r.generated += 1
-            batch.append(r)
-            slots.append(slot)
+        toks = self._next_tokens(pending)
+        i = 0
+        while i < len(pending):
+            got, done, rc = self.bm.append_slots_partial([r.rid for r in pending[i:]], toks[i:])
+            for j in range(done):
+                r, tok, slot = pending[i + j], int(toks[i + j]), int(got[j])
+                self._log("append", r.rid, tok, slot)
+                r.tokens.append(tok)
+                r.generated += 1
+                batch.append(r)
+                slots.append(slot)
+            i += done
+            if rc == 0:
+                break
+            if rc != -4:
+                raise RuntimeError("append_slot failed with status %d" % rc)
+            r = pending[i]
+            self._log("append", r.rid, int(toks[i]), None)
+            victim = self._preempt(res, batch)
+            if victim is r:
+                i += 1
+            else:
+                k = pending.index(victim)      # not yet appended: after i
+                del pending[k]
+                del toks[k]
         pairs = self.bm.take_cow_pairs()
         if pairs:
             self._log("cow", tuple(map(tuple, pairs)))
@@ -250,6 +279,13 @@ class ContinuousBatchDriver:
         self.steps += 1
         if B == 0:
             return res
+        tables, lens = self.bm.block_tables([r.rid for r in batch], max_blocks=self.max_blocks)
+        if self.grouped:
+            # members of a group must be adjacent: order the batch by first block
+            order = np.argsort(tables[:, 0], kind="stable")
+            batch = [batch[j] for j in order]
+            slots = [slots[j] for j in order]
+            tables, lens = tables[order], lens[order]
         # new tokens' K/V and queries
         if hasattr(self.src, "decode_batch"):
             k, v, q = self.src.decode_batch(batch)
@@ -264,12 +300,33 @@ class ContinuousBatchDriver:
                 self.v_new[i].copy_(v[0])
                 self.q[i].copy_(self.src.query(r, pos))
         self._write_kv(self.k_new[:B], self.v_new[:B], slots)
-        tables, lens = self.bm.block_tables([r.rid for r in batch], max_blocks=self.max_blocks)
-        tables_d = torch.from_numpy(tables).to(self.dev, non_blocking=True)
-        lens_d = torch.from_numpy(lens).to(self.dev, non_blocking=True)
-        ops.paged_attention_decode(self.out[:B], self.q[:B], self.k_cache, self.v_cache, tables_d,
-                                   lens_d, 1.0 / float(np.sqrt(self.D)),
-                                   workspace=self.workspace, dev_err=self.dev_err)
+        scale = 1.0 / float(np.sqrt(self.D))
+        groups = None
+        if self.grouped:
+            gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, self.bs,
+                                                          16 // (self.Hq // self.Hkv))
+            if mx > 0:
+                groups = (gf, sg, gs, mx, mo)
+        tables_d = self._to_device(tables)
+        lens_d = self._to_device(lens)
+        if groups is not None:
+            gf, sg, gs, mx, mo = groups
+            need = ops.grouped_workspace_bytes(B, self.Hq, self.max_blocks, mx, self.bs, self.D)
+            if self.gws is None or self.gws.numel() < need:
+                self.gws = torch.empty(max(need, 1), dtype=torch.uint8, device=self.dev)
+            meta = self._to_device(np.concatenate([gf, sg, gs]).astype(np.int32))
+            n_g = len(gs)
+            ops.paged_attention_decode_grouped(self.out[:B], self.q[:B], self.k_cache,
+                                               self.v_cache, tables_d, lens_d, meta[:n_g + 1],
+                                               meta[n_g + 1:n_g + 1 + B],
+                                               meta[n_g + 1 + B:], mx, mo, scale,
+                                               workspace=self.gws, dev_err=self.dev_err)
+            res.groups = len(gs)
+            res.shared_tokens = int(gs[sg].sum())
+        else:
+            ops.paged_attention_decode(self.out[:B], self.q[:B], self.k_cache, self.v_cache,
+                                       tables_d, lens_d, scale, workspace=self.workspace,
+                                       dev_err=self.dev_err)
         res.rids = [r.rid for r in batch]
         res.positions = [len(r.tokens) - 1 for r in batch]
         res.out = self.out[:B]
@@ -327,9 +384,11 @@ class DeviceSources:
     def query(self, req, pos):
         return torch.randn((self.Hq, self.D), generator=self.gen, device=self.dev).half()
 
+    def next_tokens(self, reqs):
+        return self.rng.integers(0, 32000, size=len(reqs)).tolist()
+
     def decode_batch(self, batch):
         B = len(batch)
-        k = torch.randn((B, self.Hkv, self.D), generator=self.gen, device=self.dev).half()
-        v = torch.randn((B, self.Hkv, self.D), generator=self.gen, device=self.dev).half()
-        q = torch.randn((B, self.Hq, self.D), generator=self.gen, device=self.dev).half()
-        return k, v, q
+        x = torch.randn((B, 2 * self.Hkv + self.Hq, self.D), generator=self.gen,
+                        device=self.dev).half()
+        return x[:, :self.Hkv], x[:, self.Hkv:2 * self.Hkv], x[:, 2 * self.Hkv:]

@@ -213,41 +213,30 @@ def swap_blocks(src_pools, dst_pools, block_pairs, dev_err=None, stream=None):
 
 
 def shared_prefix_groups(block_tables, context_lens, block_size=BLOCK_SIZE, group_size_limit=16):
-    """Host planning of grouped attention: consecutive sequences whose tables
-    start with the same physical blocks form a group (at most group_size_limit
-    members); a group shares the longest run of leading blocks every member
-    has in common with its first member, cut to a multiple of 16 tokens and of
-    the block size and to the shortest member's context.
+    """Host planning of grouped attention (native): consecutive sequences whose
+    tables start with the same physical block form a group (at most
+    group_size_limit members); a group shares the longest run of leading blocks
+    every member has in common with its first member, cut to a multiple of 16
+    tokens and of the block size and to the shortest member's context.
 
     Returns (group_first int32 [G+1], seq_group int32 [S], group_shared int32
     [G], max_shared_tokens, max_own_tokens)."""
     import numpy as np
-    tables = np.asarray(block_tables)
-    lens = np.asarray(context_lens)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
     S = len(lens)
-    unit = int(np.lcm(16, block_size))
-    first, shared, seq_group = [0], [], np.zeros(S, np.int32)
-    s = 0
-    while s < S:
-        e = s + 1
-        while (e < S and e - s < group_size_limit and lens[s] > 0 and lens[e] > 0
-               and tables[e, 0] == tables[s, 0]):
-            e += 1
-        tok = 0
-        if e - s > 1:
-            nb = min(-(-int(L) // block_size) for L in lens[s:e])
-            same = np.all(tables[s:e, :nb] == tables[s, :nb], axis=0)
-            lcp = nb if same.all() else int(np.argmin(same))
-            tok = min(lcp * block_size, int(lens[s:e].min()))
-            tok -= tok % unit
-        seq_group[s:e] = len(shared)
-        shared.append(tok)
-        first.append(e)
-        s = e
-    shared = np.array(shared, np.int32)
-    own = lens.astype(np.int64) - shared[seq_group] if S else np.zeros(0, np.int64)
-    return (np.array(first, np.int32), seq_group, shared,
-            int(shared.max()) if len(shared) else 0, int(own.max()) if S else 0)
+    first = np.empty(S + 1, np.int32)
+    seq_group = np.empty(max(S, 1), np.int32)
+    shared = np.empty(max(S, 1), np.int32)
+    ng, ms, mo = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib().pkv_plan_shared_prefix_groups(
+        p(tables), p(lens), S, tables.shape[1] if tables.ndim == 2 else 1, int(block_size),
+        int(group_size_limit), p(first), p(seq_group), p(shared), ctypes.byref(ng),
+        ctypes.byref(ms), ctypes.byref(mo))
+    check(rc, "plan_shared_prefix_groups")
+    n = ng.value
+    return first[:n + 1], seq_group[:S], shared[:n], ms.value, mo.value
 
 
 def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_shared_tokens,

@@ -59,8 +59,9 @@ def replay_on_oracle(log, num_blocks, order):
     return bm
 
 
-@pytest.mark.parametrize("preemption", ["recompute", "swap"])
-def test_driver_matches_oracle_every_step(native_lib, preemption):
+@pytest.mark.parametrize("preemption,grouped", [("recompute", False), ("swap", False),
+                                                 ("recompute", True)])
+def test_driver_matches_oracle_every_step(native_lib, preemption, grouped):
     from paged_kv_cache_138_gb300.driver import ContinuousBatchDriver, HostSources
     reqs = wl.serving_requests(SEED, num_requests=18, num_system_prompts=3,
                                system_prompt_len=40, suffix_max=12, new_min=3, new_max=60)
@@ -68,16 +69,18 @@ def test_driver_matches_oracle_every_step(native_lib, preemption):
     order = np.random.default_rng(9).permutation(nb).astype(np.int32)
     drv = ContinuousBatchDriver(nb, HQ, HKV, max_batch=6, max_blocks_per_seq=8,
                                 sources=HostSources(SEED, HQ, HKV, D), free_order=order,
-                                record_ops=True, preemption=preemption, host_blocks=64)
+                                record_ops=True, preemption=preemption, host_blocks=64,
+                                grouped=grouped)
     for r in reqs:
         drv.add_request(r.rid, r.prompt, r.max_new_tokens)
     worst, rows, steps = 0.0, 0, 0
-    cached = preempted = 0
+    cached = preempted = shared_rows = 0
     while not drv.idle:
         res = drv.step()
         steps += 1
         assert steps < 400
         cached += res.cached_tokens
+        shared_rows += res.shared_tokens
         preempted += len(res.preempted)
         if not res.rids:
             continue
@@ -92,6 +95,8 @@ def test_driver_matches_oracle_every_step(native_lib, preemption):
     assert rows == sum(r.max_new_tokens for r in reqs)   # every token decoded once
     assert cached > 0, "the trace should hit the prefix cache"
     assert preempted > 0, "the pool is sized to force preemption"
+    if grouped:
+        assert shared_rows > 0, "requests on one system prompt should be grouped"
     if preemption == "swap":
         assert drv.swapped_out_blocks > 0 and drv.swapped_in_blocks > 0
         assert len(drv.host_free) == 64
