@@ -80,30 +80,33 @@ class DecodeStep:
                         [self.v_cache[i] for i in range(self.num_layers)],
                         self.cow_pairs, dev_err=self.dev_err, stream=stream)
 
-    def run_layer(self, i, stream=None):
+    def run_layer(self, i, stream=None, bufs=None):
+        """Layer i of one step.  bufs: the step's input/output tensors (q, k_new,
+        v_new, slot_mapping, block_tables, context_lens, out); default self."""
+        b = self if bufs is None else bufs
         if self.fused:
             ops.paged_attention_decode_fused(
-                self.out[i], self.q[i], self.k_new[i], self.v_new[i], self.k_cache[i],
-                self.v_cache[i], self.block_tables, self.context_lens, self.scale,
-                workspace=self.workspace, dev_err=self.dev_err, stream=stream)
+                b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
+                b.block_tables, b.context_lens, self.scale, workspace=self.workspace,
+                dev_err=self.dev_err, stream=stream)
             return
-        ops.reshape_and_cache(self.k_new[i], self.v_new[i], self.slot_mapping, self.k_cache[i],
+        ops.reshape_and_cache(b.k_new[i], b.v_new[i], b.slot_mapping, self.k_cache[i],
                               self.v_cache[i], dev_err=self.dev_err, stream=stream)
         if self.groups is not None:
             gf, sg, gs, mx, mo = self.groups
             ops.paged_attention_decode_grouped(
-                self.out[i], self.q[i], self.k_cache[i], self.v_cache[i], self.block_tables,
-                self.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
+                b.out[i], b.q[i], self.k_cache[i], self.v_cache[i], b.block_tables,
+                b.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
                 dev_err=self.dev_err, stream=stream)
             return
-        ops.paged_attention_decode(self.out[i], self.q[i], self.k_cache[i], self.v_cache[i],
-                                   self.block_tables, self.context_lens, self.scale,
+        ops.paged_attention_decode(b.out[i], b.q[i], self.k_cache[i], self.v_cache[i],
+                                   b.block_tables, b.context_lens, self.scale,
                                    workspace=self.workspace, dev_err=self.dev_err, stream=stream)
 
-    def run(self, stream=None):
+    def run(self, stream=None, bufs=None):
         for i in range(self.num_layers):
-            self.run_layer(i, stream)
-        return self.out
+            self.run_layer(i, stream, bufs)
+        return self.out if bufs is None else bufs.out
 
     # ---- CUDA graph of one step ---------------------------------------------------
     def capture_graph(self):
@@ -169,3 +172,62 @@ class DecodeStep:
             self.run(stream=s)
             h["out"].copy_(self.out, non_blocking=True)
         return h["out"]
+
+    # ---- end to end, pipelined: copies of step i+1 overlap the kernels of step i --
+    _INPUTS = ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens")
+
+    def _pipeline(self):
+        if getattr(self, "_pipe", None) is None:
+            from types import SimpleNamespace
+            sets = []
+            for _ in range(2):
+                b = SimpleNamespace(**{n: torch.empty_like(getattr(self, n))
+                                       for n in self._INPUTS + ("out",)})
+                sets.append(b)
+            ev = lambda: torch.cuda.Event()
+            self._pipe = SimpleNamespace(
+                sets=sets, copy=torch.cuda.Stream(self.device),
+                inputs_ready=[ev(), ev()], compute_done=[ev(), ev()], out_copied=[ev(), ev()],
+                started=[False, False])
+        return self._pipe
+
+    def run_from_host_pipelined(self, host_inputs, host_outputs, stream=None):
+        """Steps k = 0 .. n-1 fed from pinned host buffers: host_inputs[k] is a
+        dict of the input tensors (names as host_buffers()), host_outputs[k] the
+        pinned output of step k.  Two device buffer sets alternate: the
+        host->device copies of step k+1 and the device->host copy of step k's
+        output run on a copy stream while step k's kernels run.  Returns after
+        enqueueing; synchronise before reading host_outputs."""
+        P = self._pipeline()
+        s = torch.cuda.current_stream(self.device) if stream is None else stream
+        n = len(host_inputs)
+
+        def upload(k):
+            j = k % 2
+            b = P.sets[j]
+            with torch.cuda.stream(P.copy):
+                if P.started[j]:
+                    P.copy.wait_event(P.compute_done[j])  # step k-2 no longer reads set j
+                for name in self._INPUTS:
+                    getattr(b, name).copy_(host_inputs[k][name], non_blocking=True)
+                P.inputs_ready[j].record(P.copy)
+
+        if n:
+            upload(0)
+        for k in range(n):
+            j = k % 2
+            b = P.sets[j]
+            if k + 1 < n:
+                upload(k + 1)
+            s.wait_event(P.inputs_ready[j])
+            if P.started[j]:
+                s.wait_event(P.out_copied[j])              # step k-2's output is on the host
+            self.apply_cow(s)
+            self.run(s, bufs=b)
+            P.compute_done[j].record(s)
+            P.started[j] = True
+            with torch.cuda.stream(P.copy):
+                P.copy.wait_event(P.compute_done[j])
+                host_outputs[k].copy_(b.out, non_blocking=True)
+                P.out_copied[j].record(P.copy)
+        return host_outputs
