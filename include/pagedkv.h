@@ -283,6 +283,17 @@ int pkv_swap_blocks(const void* const* src_pools, void* const* dst_pools, int nu
                     int64_t src_num_blocks, int64_t dst_num_blocks, int32_t* dev_err,
                     void* stream);
 
+/* ---- diagnostics ------------------------------------------------------------ */
+/*
+ * Self-test of the bounded waits the kernels use on their TMA barriers (the
+ * pages have no counterpart; it exercises this library's failure path).  One
+ * thread waits on an mbarrier that nothing arrives on; after limit_ms (1..2000)
+ * the wait gives up, stores PKV_DEV_WAIT_TIMEOUT into *dev_err (device int32,
+ * zero beforehand) and 0 into *landed (device int32), and the kernel returns:
+ * no hang, no trap, the context stays usable.
+ */
+int pkv_selftest_bounded_wait(int32_t* dev_err, int32_t* landed, int limit_ms, void* stream);
+
 /* ---- host BlockManager ---------------------------------------------------- */
 /*
  * The BlockManager of "P06 BlockManager" (free list taken FIFO, reference

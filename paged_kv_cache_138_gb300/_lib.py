@@ -42,6 +42,7 @@ SIGNATURES = {
     "pkv_reshape_and_cache": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I64, _P, _P]),
     "pkv_slot_mapping": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _P, _P]),
+    "pkv_selftest_bounded_wait": (_I, [_P, _P, _I, _P]),
     "pkv_swap_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pkv_bm_create": (_P, [_I64, _I, _I, _P]),
     "pkv_bm_destroy": (None, [_P]),

@@ -235,3 +235,29 @@ extern "C" int pkv_swap_blocks(const void* const* src_pools, void* const* dst_po
   }
   return PKV_OK;
 }
+
+// ---- self-test of the bounded wait ------------------------------------------------
+namespace pkv {
+namespace cache {
+
+// One thread waits on an mbarrier that nothing arrives on: the wait must give up
+// after limit_ns, report PKV_DEV_WAIT_TIMEOUT and return (no hang, no trap).
+__global__ void bounded_wait_selftest_kernel(int32_t* dev_err, uint64_t limit_ns,
+                                             int32_t* landed) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  *landed = mbar_wait_bounded(&bar, 0, dev_err, limit_ns) ? 1 : 0;
+}
+
+}  // namespace cache
+}  // namespace pkv
+
+extern "C" int pkv_selftest_bounded_wait(int32_t* dev_err, int32_t* landed, int limit_ms,
+                                         void* stream) {
+  if (!dev_err || !landed || limit_ms <= 0 || limit_ms > 2000) return PKV_ERR_INVALID_ARG;
+  pkv::cache::bounded_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      dev_err, static_cast<uint64_t>(limit_ms) * 1000000ull, landed);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -146,3 +146,27 @@ def test_swap_blocks_device_host_round_trip(ops):
     bad = torch.tensor([[0, 1], [hb, 2]], dtype=torch.int64, device="cuda")
     ops.swap_blocks([hk], [dk], bad, dev_err=err)
     assert ops.read_error_word(err) == 1
+
+
+def test_bounded_wait_gives_up_and_reports(ops):
+    """A barrier nothing arrives on: the wait runs out after its limit, the
+    kernel reports PKV_DEV_WAIT_TIMEOUT and returns; the GPU keeps working."""
+    import ctypes
+    import time
+    from paged_kv_cache_138_gb300._lib import lib
+    err = ops.new_error_word()
+    landed = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    t0 = time.perf_counter()
+    rc = lib().pkv_selftest_bounded_wait(ctypes.c_void_p(err.data_ptr()),
+                                         ctypes.c_void_p(landed.data_ptr()), 50, stream)
+    assert rc == 0
+    assert ops.read_error_word(err) == 4          # PKV_DEV_WAIT_TIMEOUT
+    assert int(landed.item()) == 0
+    assert time.perf_counter() - t0 < 10
+    # the context is still usable: a normal kernel runs and reports no error
+    x = torch.randn((2, 16, 1, 16), device="cuda").half()
+    err2 = ops.new_error_word()
+    ops.copy_blocks(x, x.clone(), torch.tensor([[0, 1]], dtype=torch.int64, device="cuda"),
+                    dev_err=err2)
+    assert ops.read_error_word(err2) == 0 and torch.equal(x[0], x[1])
