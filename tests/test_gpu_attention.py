@@ -157,3 +157,19 @@ def test_tiny_workload_full_step(ops):
     assert_close(out[0].cpu().numpy(), ref)
     # the cache now holds each new token at its slot
     assert np.array_equal(step.k_cache.cpu().numpy().view(np.uint16), kc.view(np.uint16))
+
+
+def test_long_context_and_many_sequences(ops):
+    """Maximum-size edges: one 65,536-token context (128 splits of 512) next to
+    short ones, and a batch of 4,096 short sequences in one launch."""
+    lengths = [65536, 1, 4097, 16]
+    q, kc, vc, tables, lens = case(11, lengths, 8, 2, extra=1)
+    gpu, code = run_gpu(ops, q, kc, vc, tables, lens, 1 / np.sqrt(D))
+    assert code == 0
+    assert_close(gpu, oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D)))
+    rng = np.random.default_rng(12)
+    lengths = rng.integers(1, 64, size=4096).tolist()
+    q, kc, vc, tables, lens = case(13, lengths, 4, 4, extra=0)
+    gpu, code = run_gpu(ops, q, kc, vc, tables, lens, 0.1)
+    assert code == 0
+    assert_close(gpu, oa.paged_attention_decode(q, kc, vc, tables, lens, 0.1))
