@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--unfused", action="store_true",
                     help="separate reshape_and_cache and attention launches per layer")
+    ap.add_argument("--driver", choices=["native", "python"], default="native",
+                    help="serving workload: native scheduler or the Python reference driver")
     ap.add_argument("--grouped", choices=["auto", "on", "off"], default="auto",
                     help="shared-prefix grouped attention (auto: on for prefix-sharing)")
     ap.add_argument("--block-size", type=int, default=16,
@@ -454,10 +456,18 @@ def run_serving(args):
     reqs = wl.serving_requests(2024, num_requests=4096, num_system_prompts=4,
                                system_prompt_len=1024, suffix_max=512, new_min=64, new_max=512)
     nb = 64 * 110
-    grouped = args.grouped != "off"
-    drv = ContinuousBatchDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
-                                sources=DeviceSources(7, Hq, Hkv), device=device,
-                                grouped=grouped)
+    grouped = args.grouped == "on"
+    native = args.driver == "native"
+    if native:
+        from paged_kv_cache_138_gb300.serving import DeviceRandomValues, NativeServingDriver
+        drv = NativeServingDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
+                                  values=DeviceRandomValues(7, Hq, Hkv, device=device),
+                                  device=device, seed=7)
+        grouped = False
+    else:
+        drv = ContinuousBatchDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
+                                    sources=DeviceSources(7, Hq, Hkv), device=device,
+                                    grouped=grouped)
     for r in reqs:
         drv.add_request(r.rid, r.prompt, r.max_new_tokens)
     import gc
@@ -474,6 +484,14 @@ def run_serving(args):
     steps = min(args.steps, 2000)
     for _ in range(steps):
         res = drv.step()
+        if native:
+            stats["seq_steps"] += len(res["rids"])
+            stats["kv_tokens"] += res["kv_tokens"]
+            stats["preempted"] += res["preempted"]
+            stats["admitted"] += res["admitted"]
+            stats["cached"] += res["cached"]
+            stats["prefill"] += res["prefill"]
+            continue
         stats["seq_steps"] += len(res.rids)
         stats["kv_tokens"] += res.kv_tokens
         stats["preempted"] += len(res.preempted)
@@ -493,7 +511,8 @@ def run_serving(args):
             "config": {"workload": "serving", "description": " ".join(
                 run_serving.__doc__.split(".")[0].split()),
                        "max_batch": 64, "pool_blocks": nb, "heads": Hq,
-                       "grouped_shared_prefix": grouped},
+                       "grouped_shared_prefix": grouped,
+                       "scheduler": "native (pkv_sched_step)" if native else "python"},
             "seq_steps_per_s": stats["seq_steps"] / wall,
             "device_ms_per_step": e0.elapsed_time(e1) / steps, "stats": stats}
     print(json.dumps(line))

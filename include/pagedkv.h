@@ -363,6 +363,65 @@ int64_t pkv_bm_ref_counts(const pkv_block_manager* bm, int32_t* out, int64_t cap
  * first one violated (1..5). */
 int pkv_bm_check_invariants(const pkv_block_manager* bm);
 
+/* ---- host continuous-batching scheduler ------------------------------------- */
+/*
+ * The per-step host work of a decode server without a model ("qaqbuyan: vLLM
+ * PagedAttention", `ContinuousBatchingScheduler.step` and `_preempt_request`;
+ * "ans20xx day 31", scheduling): release finished requests, admit waiting ones
+ * first-come first-served while the BlockManager can allocate them (prefix
+ * cache hits skip part of the prompt), append one sampled token per running
+ * request, and on OutOfBlocks preempt -- of the requests not yet decoded in
+ * this step, the one with the most generated tokens -- by recompute (requeue
+ * with its tokens; prefilled again later) or swap (its blocks go to host
+ * blocks, and come back on re-admission past the prefix-cache hits).  Tokens
+ * are drawn from a counter-based generator keyed by (seed, request, position).
+ * Host memory only; the BlockManager is borrowed and must outlive the
+ * scheduler; single-threaded.
+ */
+typedef struct pkv_scheduler pkv_scheduler;
+
+/* Caller-owned buffers one step fills, in the order the device must use them:
+ * swap-in pairs and prefill slots (admissions), swap-out pairs (preemptions),
+ * copy-on-write pairs, then the decode batch. */
+typedef struct pkv_sched_step_out {
+  int64_t* batch_rids;         /* [max_batch] sequence ids of the decode batch */
+  int32_t* positions;          /* [max_batch] position decoded (context length - 1) */
+  int32_t* tokens;             /* [max_batch] token appended */
+  int64_t* slots;              /* [max_batch] its slot */
+  int32_t* block_tables;       /* [max_batch, max_blocks_per_seq], -1 padded */
+  int32_t* context_lens;       /* [max_batch] */
+  int64_t* prefill_rids;       /* [prefill_cap] rows to write for admissions ... */
+  int32_t* prefill_positions;  /* ... their positions ... */
+  int64_t* prefill_slots;      /* ... and slots */
+  int64_t prefill_cap;         /* >= max_batch * max_blocks_per_seq * block_size */
+  int64_t* swap_in_pairs;      /* [swap_cap, 2] (host block, device block) */
+  int64_t* swap_out_pairs;     /* [swap_cap, 2] (device block, host block) */
+  int64_t swap_cap;            /* >= max_batch * max_blocks_per_seq */
+  int64_t* cow_pairs;          /* [cow_cap, 2] (src, dst) */
+  int64_t cow_cap;             /* >= max_batch */
+  int32_t num_batch, num_prefill, num_swap_in, num_swap_out, num_cow;
+  int32_t num_admitted, num_finished, num_preempted;
+  int64_t cached_tokens;       /* prompt tokens found in the prefix cache this step */
+} pkv_sched_step_out;
+
+/* preemption_swap: 0 = recompute, 1 = swap into host_blocks host blocks
+ * (falls back to recompute when they run short).  NULL on bad arguments. */
+pkv_scheduler* pkv_sched_create(pkv_block_manager* bm, int max_batch, int max_blocks_per_seq,
+                                int block_size, int preemption_swap, int64_t host_blocks,
+                                uint64_t seed, int vocab);
+void pkv_sched_destroy(pkv_scheduler* sched);
+/* Queue a request (ids unique; prompt non-empty; prompt + max_new_tokens must
+ * fit max_blocks_per_seq blocks). */
+int pkv_sched_add_request(pkv_scheduler* sched, int64_t rid, const int32_t* prompt,
+                          int64_t num_prompt_tokens, int64_t max_new_tokens);
+/* Plan one step into *out (capacities as above, checked before any change). */
+int pkv_sched_step(pkv_scheduler* sched, pkv_sched_step_out* out);
+/* Requests waiting or running. */
+int64_t pkv_sched_num_unfinished(const pkv_scheduler* sched);
+/* Tokens of a request so far (prompt + generated): the count; copies up to cap. */
+int64_t pkv_sched_request_tokens(const pkv_scheduler* sched, int64_t rid, int32_t* out,
+                                 int64_t cap);
+
 #ifdef __cplusplus
 }
 #endif

@@ -44,6 +44,12 @@ SIGNATURES = {
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _P, _P]),
     "pkv_selftest_bounded_wait": (_I, [_P, _P, _I, _P]),
     "pkv_swap_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _P]),
+    "pkv_sched_create": (_P, [_P, _I, _I, _I, _I, _I64, ctypes.c_uint64, _I]),
+    "pkv_sched_destroy": (None, [_P]),
+    "pkv_sched_add_request": (_I, [_P, _I64, _P, _I64, _I64]),
+    "pkv_sched_step": (_I, [_P, _P]),
+    "pkv_sched_num_unfinished": (_I64, [_P]),
+    "pkv_sched_request_tokens": (_I64, [_P, _I64, _P, _I64]),
     "pkv_bm_create": (_P, [_I64, _I, _I, _P]),
     "pkv_bm_destroy": (None, [_P]),
     "pkv_bm_allocate": (_I, [_P, _I64, _P, _I64, _P, _I64, _P, _P]),

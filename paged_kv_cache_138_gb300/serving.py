@@ -1,0 +1,243 @@
+"""Continuous batching with the native scheduler (pkv_sched_*) in the loop.
+
+Each step is one native call that plans everything on the host (finish, admit
+with prefix-cache hits, append a sampled token per running request, preempt by
+recompute or swap, copy-on-write, tables), followed by the device work it
+returns, in order: swap-ins and prefill writes, swap-outs, copy_blocks, the
+new tokens' reshape_and_cache and paged attention over the batch.  Python only
+marshals the arrays and launches the kernels.
+
+Values (K/V of prefill and decoded tokens, queries) come from a source object:
+``DeviceRandomValues`` draws them on the device (benchmarks);
+``ContentKeyedValues`` derives them from each request's token prefix on the
+host (tests: a block found again through the prefix cache then holds what a
+fresh prefill would write, and the oracle can recompute every row).
+"""
+import ctypes
+
+import numpy as np
+import torch
+
+from . import ops
+from . import workloads as wl
+from ._lib import PKV_OK, PagedKVError, lib
+from .block_manager import BlockManager
+
+
+class _StepOut(ctypes.Structure):
+    _fields_ = [
+        ("batch_rids", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p), ("slots", ctypes.c_void_p),
+        ("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+        ("prefill_rids", ctypes.c_void_p), ("prefill_positions", ctypes.c_void_p),
+        ("prefill_slots", ctypes.c_void_p), ("prefill_cap", ctypes.c_int64),
+        ("swap_in_pairs", ctypes.c_void_p), ("swap_out_pairs", ctypes.c_void_p),
+        ("swap_cap", ctypes.c_int64),
+        ("cow_pairs", ctypes.c_void_p), ("cow_cap", ctypes.c_int64),
+        ("num_batch", ctypes.c_int32), ("num_prefill", ctypes.c_int32),
+        ("num_swap_in", ctypes.c_int32), ("num_swap_out", ctypes.c_int32),
+        ("num_cow", ctypes.c_int32), ("num_admitted", ctypes.c_int32),
+        ("num_finished", ctypes.c_int32), ("num_preempted", ctypes.c_int32),
+        ("cached_tokens", ctypes.c_int64),
+    ]
+
+
+class NativeServingDriver:
+    def __init__(self, num_blocks, num_q_heads, num_kv_heads, max_batch, max_blocks_per_seq,
+                 values, device="cuda", block_size=16, head_dim=128, enable_prefix_cache=True,
+                 free_order=None, preemption="recompute", host_blocks=0, seed=0):
+        if preemption not in ("recompute", "swap"):
+            raise ValueError("preemption is 'recompute' or 'swap'")
+        if num_blocks < max_blocks_per_seq:
+            raise ValueError("the pool must hold at least one full-length sequence")
+        self.dev = torch.device(device)
+        self.bs, self.D, self.Hq, self.Hkv = block_size, head_dim, num_q_heads, num_kv_heads
+        self.max_batch, self.max_blocks = max_batch, max_blocks_per_seq
+        self.values = values
+        self.bm = BlockManager(num_blocks, block_size, enable_prefix_cache, free_order)
+        self._h = lib().pkv_sched_create(self.bm._h, max_batch, max_blocks_per_seq, block_size,
+                                         1 if preemption == "swap" else 0, int(host_blocks),
+                                         ctypes.c_uint64(seed), 32000)
+        if not self._h:
+            raise ValueError("pkv_sched_create rejected its arguments")
+        shape = (num_blocks, block_size, num_kv_heads, head_dim)
+        self.k_cache = torch.zeros(shape, dtype=torch.float16, device=self.dev)
+        self.v_cache = torch.zeros_like(self.k_cache)
+        self.host_k = self.host_v = None
+        if preemption == "swap" and host_blocks:
+            hs = (host_blocks,) + shape[1:]
+            self.host_k = torch.empty(hs, dtype=torch.float16, pin_memory=True)
+            self.host_v = torch.empty(hs, dtype=torch.float16, pin_memory=True)
+        B, mb = max_batch, max_blocks_per_seq
+        # Two sets of step arrays in pinned host memory, used alternately: the
+        # scheduler writes set k % 2 while the device may still be copying set
+        # (k - 1) % 2; set reuse waits on the event recorded after its copies.
+        pin = self.dev.type == "cuda"
+        spec = {
+            "batch_rids": ((B,), torch.int64), "positions": ((B,), torch.int32),
+            "tokens": ((B,), torch.int32), "slots": ((B,), torch.int64),
+            "block_tables": ((B, mb), torch.int32), "context_lens": ((B,), torch.int32),
+            "prefill_rids": ((B * mb * block_size,), torch.int64),
+            "prefill_positions": ((B * mb * block_size,), torch.int32),
+            "prefill_slots": ((B * mb * block_size,), torch.int64),
+            "swap_in_pairs": ((B * mb, 2), torch.int64),
+            "swap_out_pairs": ((B * mb, 2), torch.int64),
+            "cow_pairs": ((B, 2), torch.int64),
+        }
+        self.sets = []
+        for _ in range(2):
+            t = {n: torch.zeros(shape, dtype=dt, pin_memory=pin) for n, (shape, dt) in spec.items()}
+            o = _StepOut()
+            for name, ten in t.items():
+                setattr(o, name, ctypes.c_void_p(ten.data_ptr()))
+            o.prefill_cap = B * mb * block_size
+            o.swap_cap = B * mb
+            o.cow_cap = B
+            ev = torch.cuda.Event() if pin else None
+            self.sets.append({"t": t, "a": {n: x.numpy() for n, x in t.items()}, "out": o,
+                              "event": ev, "used": False})
+        self.out = torch.empty((B, num_q_heads, head_dim), dtype=torch.float16, device=self.dev)
+        self.k_new = torch.empty((B, num_kv_heads, head_dim), dtype=torch.float16,
+                                 device=self.dev)
+        self.v_new = torch.empty_like(self.k_new)
+        self.q = torch.empty_like(self.out)
+        self.workspace = ops.alloc_workspace(B, num_q_heads, mb, self.dev, block_size)
+        self.dev_err = ops.new_error_word(self.dev)
+        self.scale = 1.0 / float(np.sqrt(head_dim))
+        self.steps = 0
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            lib().pkv_sched_destroy(h)
+            self._h = None
+
+    def add_request(self, rid, prompt, max_new_tokens):
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        rc = lib().pkv_sched_add_request(self._h, int(rid), p.ctypes.data_as(ctypes.c_void_p),
+                                         len(p), int(max_new_tokens))
+        if rc != PKV_OK:
+            raise PagedKVError(rc, "add_request")
+
+    @property
+    def idle(self):
+        return lib().pkv_sched_num_unfinished(self._h) == 0
+
+    def request_tokens(self, rid):
+        n = lib().pkv_sched_request_tokens(self._h, int(rid), None, 0)
+        if n < 0:
+            raise PagedKVError(int(n), "request_tokens")
+        out = np.empty(max(n, 1), np.int32)
+        lib().pkv_sched_request_tokens(self._h, int(rid), out.ctypes.data_as(ctypes.c_void_p), n)
+        return out[:n]
+
+    def _to_device(self, arr):
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+        if self.dev.type == "cuda":
+            t = t.pin_memory()
+        return t.to(self.dev, non_blocking=True)
+
+    def _h2d(self, t):
+        return t.to(self.dev, non_blocking=True)
+
+    def step(self):
+        """Plan and launch one step.  Returns a dict with the decode batch's ids,
+        positions, the output rows (device, valid until the next step) and
+        counters."""
+        st = self.sets[self.steps % 2]
+        if st["used"] and st["event"] is not None:
+            st["event"].synchronize()           # its copies from two steps ago are done
+        o, t, a = st["out"], st["t"], st["a"]
+        rc = lib().pkv_sched_step(self._h, ctypes.byref(o))
+        if rc != PKV_OK:
+            raise PagedKVError(rc, "sched_step")
+        caches = ([self.k_cache, self.v_cache], [self.host_k, self.host_v])
+        if o.num_swap_in:
+            ops.swap_blocks(caches[1], caches[0], self._h2d(t["swap_in_pairs"][:o.num_swap_in]),
+                            dev_err=self.dev_err)
+        if o.num_prefill:
+            n = o.num_prefill
+            k, v = self.values.prefill(self, a["prefill_rids"][:n], a["prefill_positions"][:n])
+            ops.reshape_and_cache(k, v, self._h2d(t["prefill_slots"][:n]), self.k_cache,
+                                  self.v_cache, dev_err=self.dev_err)
+        if o.num_swap_out:
+            ops.swap_blocks(caches[0], caches[1], self._h2d(t["swap_out_pairs"][:o.num_swap_out]),
+                            dev_err=self.dev_err)
+        if o.num_cow:
+            ops.copy_blocks(self.k_cache, self.v_cache, self._h2d(t["cow_pairs"][:o.num_cow]),
+                            dev_err=self.dev_err)
+        B = o.num_batch
+        res = {"rids": a["batch_rids"][:B].copy(), "positions": a["positions"][:B].copy(),
+               "out": self.out[:B], "admitted": o.num_admitted, "finished": o.num_finished,
+               "preempted": o.num_preempted, "prefill": o.num_prefill,
+               "cached": int(o.cached_tokens), "swap_in": o.num_swap_in,
+               "swap_out": o.num_swap_out, "kv_tokens": int(a["context_lens"][:B].sum())}
+        if B:
+            self.values.decode_into(self, res["rids"], res["positions"], self.k_new[:B],
+                                    self.v_new[:B], self.q[:B])
+            ops.reshape_and_cache(self.k_new[:B], self.v_new[:B], self._h2d(t["slots"][:B]),
+                                  self.k_cache, self.v_cache, dev_err=self.dev_err)
+            ops.paged_attention_decode(self.out[:B], self.q[:B], self.k_cache, self.v_cache,
+                                       self._h2d(t["block_tables"][:B]),
+                                       self._h2d(t["context_lens"][:B]), self.scale,
+                                       workspace=self.workspace, dev_err=self.dev_err)
+        if st["event"] is not None:
+            st["event"].record()
+        st["used"] = True
+        self.steps += 1
+        return res
+
+    def check_errors(self):
+        code = ops.read_error_word(self.dev_err)
+        if code:
+            raise RuntimeError("device reported error code %d" % code)
+
+
+class DeviceRandomValues:
+    """K/V/q drawn on the device (one generator launch per kind per step)."""
+
+    def __init__(self, seed, num_q_heads, num_kv_heads, head_dim=128, device="cuda"):
+        self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
+        self.gen = torch.Generator(device=device)
+        self.gen.manual_seed(seed)
+        self.dev = device
+
+    def prefill(self, drv, rids, positions):
+        x = torch.randn((2, len(rids), self.Hkv, self.D), generator=self.gen,
+                        device=self.dev).half()
+        return x[0], x[1]
+
+    def decode_into(self, drv, rids, positions, k, v, q):
+        for t in (k, v, q):
+            t.normal_(generator=self.gen)
+
+
+class ContentKeyedValues:
+    """K/V of a token = a function of the request's token prefix; q of a decode
+    step = a function of (request, position).  Host-side, for tests."""
+
+    def __init__(self, seed, num_q_heads, num_kv_heads, head_dim=128, device="cuda"):
+        self.seed, self.Hq, self.Hkv, self.D, self.dev = seed, num_q_heads, num_kv_heads, \
+            head_dim, device
+
+    def _kv(self, drv, rids, positions):
+        ks, vs, cache = [], [], {}
+        for rid, pos in zip(rids.tolist(), positions.tolist()):
+            if rid not in cache:
+                cache[rid] = wl.prefix_keys(drv.request_tokens(rid), self.seed)
+            k, v = wl.token_kv_host([cache[rid][pos]], self.Hkv, self.D)
+            ks.append(k[0])
+            vs.append(v[0])
+        return (torch.from_numpy(np.stack(ks)).to(self.dev),
+                torch.from_numpy(np.stack(vs)).to(self.dev))
+
+    def prefill(self, drv, rids, positions):
+        return self._kv(drv, rids, positions)
+
+    def decode_into(self, drv, rids, positions, k_out, v_out, q_out):
+        k, v = self._kv(drv, rids, positions)
+        q = np.stack([wl.step_query_host(self.seed, r, p, self.Hq, self.D)
+                      for r, p in zip(rids.tolist(), positions.tolist())])
+        k_out.copy_(k)
+        v_out.copy_(v)
+        q_out.copy_(torch.from_numpy(q))
