@@ -460,10 +460,10 @@ def run_serving(args):
     native = args.driver == "native"
     if native:
         from paged_kv_cache_138_gb300.serving import DeviceRandomValues, NativeServingDriver
+        grouped = args.grouped != "off"
         drv = NativeServingDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
                                   values=DeviceRandomValues(7, Hq, Hkv, device=device),
-                                  device=device, seed=7)
-        grouped = False
+                                  device=device, seed=7, grouped=grouped)
     else:
         drv = ContinuousBatchDriver(nb, Hq, Hkv, max_batch=64, max_blocks_per_seq=160,
                                     sources=DeviceSources(7, Hq, Hkv), device=device,
@@ -485,6 +485,7 @@ def run_serving(args):
     for _ in range(steps):
         res = drv.step()
         if native:
+            stats["shared_tokens"] += res["shared_tokens"]
             stats["seq_steps"] += len(res["rids"])
             stats["kv_tokens"] += res["kv_tokens"]
             stats["preempted"] += res["preempted"]

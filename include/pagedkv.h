@@ -399,6 +399,14 @@ typedef struct pkv_sched_step_out {
   int64_t swap_cap;            /* >= max_batch * max_blocks_per_seq */
   int64_t* cow_pairs;          /* [cow_cap, 2] (src, dst) */
   int64_t cow_cap;             /* >= max_batch */
+  /* Shared-prefix groups of the decode batch (pkv_paged_attention_decode_grouped):
+   * with group_limit > 0 the batch is ordered by first physical block and
+   * planned as pkv_plan_shared_prefix_groups does; 0 leaves it unplanned. */
+  int32_t group_limit;         /* in: at most this many members per group */
+  int32_t* group_first;        /* [max_batch + 1] */
+  int32_t* seq_group;          /* [max_batch] */
+  int32_t* group_shared;       /* [max_batch] */
+  int32_t num_groups, max_shared_tokens, max_own_tokens;
   int32_t num_batch, num_prefill, num_swap_in, num_swap_out, num_cow;
   int32_t num_admitted, num_finished, num_preempted;
   int64_t cached_tokens;       /* prompt tokens found in the prefix cache this step */
@@ -416,6 +424,36 @@ int pkv_sched_add_request(pkv_scheduler* sched, int64_t rid, const int32_t* prom
                           int64_t num_prompt_tokens, int64_t max_new_tokens);
 /* Plan one step into *out (capacities as above, checked before any change). */
 int pkv_sched_step(pkv_scheduler* sched, pkv_sched_step_out* out);
+/* Device side of a step's decode batch, for pkv_sched_launch_decode. */
+typedef struct pkv_decode_launch {
+  void* k_cache;               /* fp16 [num_blocks, block_size, num_kv_heads, head_dim] */
+  void* v_cache;
+  int64_t num_blocks;
+  int num_q_heads, num_kv_heads, head_dim;
+  const void* q;               /* fp16 [max_batch, num_q_heads, head_dim], rows of the batch */
+  const void* k_new;           /* fp16 [max_batch, num_kv_heads, head_dim] */
+  const void* v_new;
+  void* out;                   /* fp16 [max_batch, num_q_heads, head_dim] */
+  void* meta;                  /* device staging for the step's metadata ... */
+  size_t meta_bytes;           /* ... of at least pkv_sched_meta_bytes() */
+  void* workspace;             /* attention workspace (grouped size when grouping) */
+  size_t workspace_bytes;
+  float scale;
+  int32_t* dev_err;
+} pkv_decode_launch;
+
+/* Device staging bytes pkv_sched_launch_decode needs. */
+size_t pkv_sched_meta_bytes(const pkv_scheduler* sched);
+
+/* Enqueue the decode part of a planned step on `stream`: copy the batch's
+ * slots, block tables, context lengths and groups from out's (pinned) arrays
+ * to d->meta, write the new tokens' K/V at their slots, and run paged
+ * attention -- grouped when the step planned shared-prefix groups.  The
+ * caller has filled q / k_new / v_new for rows 0 .. out->num_batch - 1 and
+ * enqueued the step's swaps, prefill writes and copies before. */
+int pkv_sched_launch_decode(const pkv_scheduler* sched, const pkv_sched_step_out* out,
+                            const pkv_decode_launch* d, void* stream);
+
 /* Requests waiting or running. */
 int64_t pkv_sched_num_unfinished(const pkv_scheduler* sched);
 /* Tokens of a request so far (prompt + generated): the count; copies up to cap. */

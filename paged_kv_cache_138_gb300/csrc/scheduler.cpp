@@ -17,6 +17,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <cuda_runtime.h>
+
 #include "pagedkv.h"
 
 namespace {
@@ -260,15 +262,108 @@ int pkv_sched_step(pkv_scheduler* s, pkv_sched_step_out* o) {
     if (ncow > o->cow_cap) return PKV_ERR_INVALID_ARG;
     if (ncow > 0) pkv_bm_take_cow_pairs(s->bm, o->cow_pairs, o->cow_cap);
     o->num_cow = static_cast<int32_t>(ncow);
-    if (o->num_batch > 0) {
-      const int rc = pkv_bm_fill_block_tables(s->bm, o->batch_rids, o->num_batch, o->block_tables,
+    o->num_groups = o->max_shared_tokens = o->max_own_tokens = 0;
+    const int B = o->num_batch;
+    if (B > 0) {
+      const int rc = pkv_bm_fill_block_tables(s->bm, o->batch_rids, B, o->block_tables,
                                               s->max_blocks, -1, o->context_lens);
       if (rc != PKV_OK) return rc;
+    }
+    if (B > 0 && o->group_limit > 0) {
+      // order the batch by first physical block so requests sharing a prompt
+      // (prefix-cache hits) sit together, then plan their groups
+      const int mb = s->max_blocks;
+      std::vector<int> order(static_cast<size_t>(B));
+      for (int b = 0; b < B; ++b) order[b] = b;
+      std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+        return o->block_tables[static_cast<int64_t>(x) * mb] <
+               o->block_tables[static_cast<int64_t>(y) * mb];
+      });
+      std::vector<int64_t> rids(o->batch_rids, o->batch_rids + B), slots(o->slots, o->slots + B);
+      std::vector<int32_t> pos(o->positions, o->positions + B), toks(o->tokens, o->tokens + B),
+          lens(o->context_lens, o->context_lens + B),
+          tabs(o->block_tables, o->block_tables + static_cast<int64_t>(B) * mb);
+      for (int b = 0; b < B; ++b) {
+        const int src = order[b];
+        o->batch_rids[b] = rids[src];
+        o->slots[b] = slots[src];
+        o->positions[b] = pos[src];
+        o->tokens[b] = toks[src];
+        o->context_lens[b] = lens[src];
+        std::memcpy(o->block_tables + static_cast<int64_t>(b) * mb,
+                    tabs.data() + static_cast<int64_t>(src) * mb, sizeof(int32_t) * mb);
+      }
+      if (!o->group_first || !o->seq_group || !o->group_shared) return PKV_ERR_INVALID_ARG;
+      int ng = 0, ms = 0, mo = 0;
+      const int rc = pkv_plan_shared_prefix_groups(o->block_tables, o->context_lens, B, mb,
+                                                   s->block_size, o->group_limit, o->group_first,
+                                                   o->seq_group, o->group_shared, &ng, &ms, &mo);
+      if (rc != PKV_OK) return rc;
+      o->num_groups = ng;
+      o->max_shared_tokens = ms;
+      o->max_own_tokens = mo;
     }
     return PKV_OK;
   } catch (...) {
     return PKV_ERR_INVALID_ARG;
   }
+}
+
+
+size_t pkv_sched_meta_bytes(const pkv_scheduler* s) {
+  if (!s) return 0;
+  const size_t B = static_cast<size_t>(s->max_batch);
+  // slots (int64), then int32: tables, context lengths, groups (3 B + 1)
+  return B * 8 + (B * s->max_blocks + B + 3 * B + 1) * 4 + 64;
+}
+
+int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
+                            const pkv_decode_launch* d, void* stream) {
+  if (!s || !o || !d || !d->meta || d->meta_bytes < pkv_sched_meta_bytes(s))
+    return PKV_ERR_INVALID_ARG;
+  const int B = o->num_batch;
+  if (B == 0) return PKV_OK;
+  const int mb = s->max_blocks;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* meta = static_cast<uint8_t*>(d->meta);
+  int64_t* slots = reinterpret_cast<int64_t*>(meta);
+  int32_t* tables = reinterpret_cast<int32_t*>(meta + static_cast<size_t>(s->max_batch) * 8);
+  int32_t* lens = tables + static_cast<size_t>(s->max_batch) * mb;
+  int32_t* groups = lens + s->max_batch;  // group_first | seq_group | group_shared
+  const bool grouped = o->num_groups > 0 && o->max_shared_tokens > 0;
+  if (cudaMemcpyAsync(slots, o->slots, sizeof(int64_t) * B, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return PKV_ERR_CUDA;
+  int32_t* gfirst = groups;
+  int32_t* gseq = groups + s->max_batch + 1;
+  int32_t* gshared = gseq + s->max_batch;
+  if (grouped) {
+    if (cudaMemcpyAsync(gfirst, o->group_first, sizeof(int32_t) * (o->num_groups + 1),
+                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(gseq, o->seq_group, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(gshared, o->group_shared, sizeof(int32_t) * o->num_groups,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return PKV_ERR_CUDA;
+  }
+  int rc = pkv_reshape_and_cache(d->k_new, d->v_new, slots, d->k_cache, d->v_cache, B,
+                                 d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks,
+                                 d->dev_err, stream);
+  if (rc != PKV_OK) return rc;
+  if (grouped)
+    return pkv_paged_attention_decode_grouped(
+        d->out, d->q, d->k_cache, d->v_cache, tables, lens, gfirst, gseq, gshared,
+        o->num_groups, o->max_shared_tokens, o->max_own_tokens, B, d->num_q_heads,
+        d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks, mb, d->scale, d->workspace,
+        d->workspace_bytes, d->dev_err, stream);
+  return pkv_paged_attention_decode(d->out, d->q, d->k_cache, d->v_cache, tables, lens, B,
+                                    d->num_q_heads, d->num_kv_heads, d->head_dim, s->block_size,
+                                    d->num_blocks, mb, d->scale, d->workspace,
+                                    d->workspace_bytes, d->dev_err, stream);
 }
 
 }  // extern "C"

@@ -34,6 +34,10 @@ class _StepOut(ctypes.Structure):
         ("swap_in_pairs", ctypes.c_void_p), ("swap_out_pairs", ctypes.c_void_p),
         ("swap_cap", ctypes.c_int64),
         ("cow_pairs", ctypes.c_void_p), ("cow_cap", ctypes.c_int64),
+        ("group_limit", ctypes.c_int32), ("group_first", ctypes.c_void_p),
+        ("seq_group", ctypes.c_void_p), ("group_shared", ctypes.c_void_p),
+        ("num_groups", ctypes.c_int32), ("max_shared_tokens", ctypes.c_int32),
+        ("max_own_tokens", ctypes.c_int32),
         ("num_batch", ctypes.c_int32), ("num_prefill", ctypes.c_int32),
         ("num_swap_in", ctypes.c_int32), ("num_swap_out", ctypes.c_int32),
         ("num_cow", ctypes.c_int32), ("num_admitted", ctypes.c_int32),
@@ -42,10 +46,21 @@ class _StepOut(ctypes.Structure):
     ]
 
 
+class _DecodeLaunch(ctypes.Structure):
+    _fields_ = [
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int64),
+        ("num_q_heads", ctypes.c_int), ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("meta", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("scale", ctypes.c_float), ("dev_err", ctypes.c_void_p),
+    ]
+
+
 class NativeServingDriver:
     def __init__(self, num_blocks, num_q_heads, num_kv_heads, max_batch, max_blocks_per_seq,
                  values, device="cuda", block_size=16, head_dim=128, enable_prefix_cache=True,
-                 free_order=None, preemption="recompute", host_blocks=0, seed=0):
+                 free_order=None, preemption="recompute", host_blocks=0, seed=0, grouped=False):
         if preemption not in ("recompute", "swap"):
             raise ValueError("preemption is 'recompute' or 'swap'")
         if num_blocks < max_blocks_per_seq:
@@ -83,13 +98,20 @@ class NativeServingDriver:
             "swap_in_pairs": ((B * mb, 2), torch.int64),
             "swap_out_pairs": ((B * mb, 2), torch.int64),
             "cow_pairs": ((B, 2), torch.int64),
+            "groups": ((3 * B + 1,), torch.int32),   # group_first | seq_group | group_shared
         }
         self.sets = []
         for _ in range(2):
             t = {n: torch.zeros(shape, dtype=dt, pin_memory=pin) for n, (shape, dt) in spec.items()}
             o = _StepOut()
             for name, ten in t.items():
-                setattr(o, name, ctypes.c_void_p(ten.data_ptr()))
+                if name != "groups":
+                    setattr(o, name, ctypes.c_void_p(ten.data_ptr()))
+            g = t["groups"]
+            o.group_first = ctypes.c_void_p(g.data_ptr())
+            o.seq_group = ctypes.c_void_p(g[B + 1:].data_ptr())
+            o.group_shared = ctypes.c_void_p(g[2 * B + 1:].data_ptr())
+            o.group_limit = 16 // (num_q_heads // num_kv_heads) if grouped else 0
             o.prefill_cap = B * mb * block_size
             o.swap_cap = B * mb
             o.cow_cap = B
@@ -101,10 +123,33 @@ class NativeServingDriver:
                                  device=self.dev)
         self.v_new = torch.empty_like(self.k_new)
         self.q = torch.empty_like(self.out)
-        self.workspace = ops.alloc_workspace(B, num_q_heads, mb, self.dev, block_size)
+        self.grouped = bool(grouped)
+        if self.grouped:
+            n = ops.grouped_workspace_bytes(B, num_q_heads, mb, mb * block_size, block_size,
+                                            head_dim)
+            self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
+        else:
+            self.workspace = ops.alloc_workspace(B, num_q_heads, mb, self.dev, block_size)
         self.dev_err = ops.new_error_word(self.dev)
         self.scale = 1.0 / float(np.sqrt(head_dim))
         self.steps = 0
+        # the decode launch: one native call per step (metadata copies, cache
+        # write, plain or grouped attention)
+        self.meta = torch.empty(int(lib().pkv_sched_meta_bytes(self._h)), dtype=torch.uint8,
+                                device=self.dev)
+        dl = _DecodeLaunch()
+        dl.k_cache, dl.v_cache = self.k_cache.data_ptr(), self.v_cache.data_ptr()
+        dl.num_blocks = num_blocks
+        dl.num_q_heads, dl.num_kv_heads, dl.head_dim = num_q_heads, num_kv_heads, head_dim
+        dl.q, dl.k_new, dl.v_new = self.q.data_ptr(), self.k_new.data_ptr(), self.v_new.data_ptr()
+        dl.out = self.out.data_ptr()
+        dl.meta, dl.meta_bytes = self.meta.data_ptr(), self.meta.numel()
+        ws = self.workspace
+        dl.workspace = ws.data_ptr() if ws is not None else None
+        dl.workspace_bytes = ws.numel() if ws is not None else 0
+        dl.scale = self.scale
+        dl.dev_err = self.dev_err.data_ptr()
+        self.launch = dl
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -171,16 +216,22 @@ class NativeServingDriver:
                "out": self.out[:B], "admitted": o.num_admitted, "finished": o.num_finished,
                "preempted": o.num_preempted, "prefill": o.num_prefill,
                "cached": int(o.cached_tokens), "swap_in": o.num_swap_in,
-               "swap_out": o.num_swap_out, "kv_tokens": int(a["context_lens"][:B].sum())}
+               "swap_out": o.num_swap_out, "kv_tokens": int(a["context_lens"][:B].sum()),
+               "groups": 0, "shared_tokens": 0}
         if B:
             self.values.decode_into(self, res["rids"], res["positions"], self.k_new[:B],
                                     self.v_new[:B], self.q[:B])
-            ops.reshape_and_cache(self.k_new[:B], self.v_new[:B], self._h2d(t["slots"][:B]),
-                                  self.k_cache, self.v_cache, dev_err=self.dev_err)
-            ops.paged_attention_decode(self.out[:B], self.q[:B], self.k_cache, self.v_cache,
-                                       self._h2d(t["block_tables"][:B]),
-                                       self._h2d(t["context_lens"][:B]), self.scale,
-                                       workspace=self.workspace, dev_err=self.dev_err)
+            rc = lib().pkv_sched_launch_decode(
+                self._h, ctypes.byref(o), ctypes.byref(self.launch),
+                ctypes.c_void_p(torch.cuda.current_stream(self.dev).cuda_stream)
+                if self.dev.type == "cuda" else None)
+            if rc != PKV_OK:
+                raise PagedKVError(rc, "sched_launch_decode")
+            if o.num_groups and o.max_shared_tokens > 0:
+                g = a["groups"]
+                res["groups"] = o.num_groups
+                res["shared_tokens"] = int(g[2 * self.max_batch + 1:][
+                    g[self.max_batch + 1:self.max_batch + 1 + B]].sum())
         if st["event"] is not None:
             st["event"].record()
         st["used"] = True

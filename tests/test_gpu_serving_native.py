@@ -25,8 +25,9 @@ def oracle_row(tokens, rid, pos):
                                      np.array([n], np.int32), 1 / np.sqrt(D))[0]
 
 
-@pytest.mark.parametrize("preemption", ["recompute", "swap"])
-def test_native_serving_matches_oracle_every_step(native_lib, preemption):
+@pytest.mark.parametrize("preemption,grouped", [("recompute", False), ("swap", False),
+                                                 ("recompute", True), ("swap", True)])
+def test_native_serving_matches_oracle_every_step(native_lib, preemption, grouped):
     from paged_kv_cache_138_gb300.serving import ContentKeyedValues, NativeServingDriver
     reqs = wl.serving_requests(SEED, num_requests=18, num_system_prompts=3,
                                system_prompt_len=40, suffix_max=12, new_min=3, new_max=60)
@@ -34,11 +35,12 @@ def test_native_serving_matches_oracle_every_step(native_lib, preemption):
     drv = NativeServingDriver(nb, HQ, HKV, max_batch=6, max_blocks_per_seq=8,
                               values=ContentKeyedValues(SEED, HQ, HKV, D),
                               free_order=np.random.default_rng(9).permutation(nb),
-                              preemption=preemption, host_blocks=64, seed=SEED)
+                              preemption=preemption, host_blocks=64, seed=SEED,
+                              grouped=grouped)
     for r in reqs:
         drv.add_request(r.rid, r.prompt, r.max_new_tokens)
     worst, rows, steps = 0.0, 0, 0
-    stats = {"preempted": 0, "cached": 0, "swap_out": 0, "swap_in": 0}
+    stats = {"preempted": 0, "cached": 0, "swap_out": 0, "swap_in": 0, "shared_tokens": 0}
     while not drv.idle:
         res = drv.step()
         steps += 1
@@ -58,5 +60,7 @@ def test_native_serving_matches_oracle_every_step(native_lib, preemption):
     assert stats["cached"] > 0 and stats["preempted"] > 0
     if preemption == "swap":
         assert stats["swap_out"] > 0 and stats["swap_in"] > 0
+    if grouped:
+        assert stats["shared_tokens"] > 0
     drv.bm.check_invariants()
     assert drv.bm.num_free_blocks == nb
