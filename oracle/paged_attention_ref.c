@@ -13,7 +13,7 @@
  *   - "P06 BlockManager", problem summary: token `pos` lives at
  *     slot = table[pos // bs] * bs + pos % bs, i.e. physical block table[pos // bs],
  *     row pos % bs of that block.
- * Readings taken where the pages are silent (listed in the design doc as well):
+ * Readings taken where the pages are silent:
  *   - exactly context_lens[s] tokens are attended (the page's CUDA sketch would
  *     attend every row of the last block; its signature has no length mask);
  *   - query head h reads KV head h / (Hq / Hkv) (contiguous GQA groups);
