@@ -80,6 +80,7 @@ struct Params {
   int64_t num_blocks;
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
+  int seq_stride;     // split grid: row y of the grid is sequence (y * seq_stride) % S
   float scale_log2;
 };
 
@@ -614,13 +615,18 @@ __device__ __forceinline__ uint8_t* aligned_smem() {
   return smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
 }
 
-// grid (KV heads, sequences, splits)
+// grid (KV heads, sequences, splits).  CTAs start in grid order, so a batch
+// ordered by length (as continuous batching tends to keep it: older requests
+// are longer) would start all its short units back to back, and a CTA with a
+// short unit spends most of its life in set-up and merge.  Row y of the grid
+// therefore takes sequence (y * seq_stride) % S, a stride coprime with S
+// near 0.618 S, which spreads neighbours in the batch across the grid.
 template <int G, int BS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
-  split_body<G, BS, FUSED>(tmap_k, tmap_v, p, aligned_smem(), blockIdx.x, blockIdx.y,
-                           blockIdx.z);
+  const int s = static_cast<int>(static_cast<int64_t>(blockIdx.y) * p.seq_stride % p.num_seqs);
+  split_body<G, BS, FUSED>(tmap_k, tmap_v, p, aligned_smem(), blockIdx.x, s, blockIdx.z);
 }
 
 // One launch for a grouped step, 1-D grid: first the shared-prefix units

@@ -73,6 +73,25 @@ bool make_cache_map(CUtensorMap* map, const void* base, int num_kv_heads, int64_
 
 bool supported_block_size(int bs) { return bs == 8 || bs == 16 || bs == 32 || bs == 64; }
 
+// Stride of the split grid's sequence order: the first value coprime with S
+// at or above 0.618 S (1 for S <= 2), so that y -> y * stride % S permutes the
+// sequences and batch neighbours land far apart.
+int seq_stride_for(int num_seqs) {
+  if (num_seqs <= 2) return 1;
+  auto gcd = [](int a, int b) {
+    while (b) {
+      const int t = a % b;
+      a = b;
+      b = t;
+    }
+    return a;
+  };
+  int k = static_cast<int>(0.618 * num_seqs);
+  if (k < 1) k = 1;
+  while (gcd(k, num_seqs) != 1) ++k;
+  return k;
+}
+
 // Shared validation + launch of both entry points.
 struct Groups {
   const int32_t* first = nullptr;
@@ -157,6 +176,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.num_groups = groups.num_groups;
   p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
                     kPartitionTiles * kPartitionTiles;
+  p.seq_stride = seq_stride_for(num_seqs);
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap mk, mv;

@@ -125,8 +125,10 @@ class NativeServingDriver:
         self.q = torch.empty_like(self.out)
         self.grouped = bool(grouped)
         if self.grouped:
-            n = ops.grouped_workspace_bytes(B, num_q_heads, mb, mb * block_size, block_size,
-                                            head_dim)
+            # steps without a shared prefix run the plain entry point on the same buffer
+            n = max(ops.grouped_workspace_bytes(B, num_q_heads, mb, mb * block_size, block_size,
+                                                head_dim),
+                    ops.workspace_bytes(B, num_q_heads, mb, block_size, head_dim))
             self.workspace = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
         else:
             self.workspace = ops.alloc_workspace(B, num_q_heads, mb, self.dev, block_size)
