@@ -105,6 +105,21 @@ def test_permutation_of_placement_is_bit_exact(ops):
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+def test_batch_order_does_not_change_any_bit(ops):
+    """A sequence's splits depend on its own length only, so reordering the
+    batch (sorted by length, then longest first) permutes the output rows bit
+    for bit, whichever grid row each sequence lands on."""
+    rng = np.random.default_rng(14)
+    lengths = rng.integers(1, 3000, size=24).tolist()
+    q, kc, vc, tables, lens = case(15, lengths, 32, 8)
+    a, code = run_gpu(ops, q, kc, vc, tables, lens, 0.1)
+    assert code == 0
+    for order in (np.argsort(lens), np.argsort(lens)[::-1].copy()):
+        b, code = run_gpu(ops, q[order], kc, vc, tables[order], lens[order], 0.1)
+        assert code == 0
+        assert np.array_equal(b.view(np.uint16), a[order].view(np.uint16))
+
+
 def test_identity_table_equals_contiguous_layout(ops):
     # one sequence whose blocks are 0..n-1 in order: the paged kernel must give
     # what torch's dense attention gives on the same contiguous K/V
