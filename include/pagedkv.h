@@ -85,7 +85,13 @@ int pkv_version(void);
  *              Contents need no initialisation.  Two launches in flight at
  *              once must not share a workspace.
  *   dev_err    device int32 (see above); may be NULL to skip reporting.
- * fp32 accumulation throughout; the result is rounded to fp16 once.
+ * fp32 accumulation throughout; the result is rounded to fp16 once.  Long
+ * contexts are cut into splits of 2048, 1024 or 512 tokens, the longest that
+ * still gives num_seqs x num_kv_heads x ceil(max_blocks_per_seq * block_size /
+ * split) >= 1024 CTAs; their partials are merged by log-sum-exp.  A
+ * sequence's output bits therefore depend on its own length and on those
+ * launch sizes only: not on block ids, the order of the batch or the other
+ * sequences' lengths.
  */
 int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                const void* v_cache, const int32_t* block_tables,

@@ -9,7 +9,11 @@
 //
 // How (GB300 design, not the pages' sketch):
 //  * The unit of work is a 16-token tile.  One CTA per (KV head g, sequence s,
-//    split of up to 32 tiles = 512 tokens).  The G = Hq / Hkv query heads that
+//    split of up to T tiles), T = 128, 64 or 32 (2048, 1024 or 512 tokens) per
+//    launch: the largest that still gives the grid enough CTAs (see
+//    partition_tiles_for).  A CTA's set-up, drain and cross-warp merge cost the
+//    same whatever its length, so long splits amortise them; a batch too small
+//    to fill the GPU with long splits gets short ones.  The G = Hq / Hkv query heads that
 //    read KV head g are handled together, so every K/V byte leaves HBM once.
 //  * Each of the 4 warps streams its own tiles of the split (warp w takes tiles
 //    w, w+4, ...) through a private 3-stage ring in shared memory.  A stage is
@@ -45,7 +49,8 @@ constexpr int kTile = 16;                          // tokens per stage
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kStages = 3;
-constexpr int kPartitionTiles = 32;                // tiles per CTA split (512 tokens)
+constexpr int kPartitionTiles = 32;                // shortest split T (512 tokens)
+constexpr int kMaxPartitionTiles = 128;            // longest split: 32 tiles per warp
 constexpr int kHalfTileBytes = kTile * 64 * 2;     // 16 rows x 128 B
 constexpr int kStageBytes = 4 * kHalfTileBytes;    // K lo, K hi, V lo, V hi
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
@@ -81,13 +86,25 @@ struct Params {
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
   int seq_stride;     // split grid: row y of the grid is sequence (y * seq_stride) % S
+  int partition_tiles;  // T: tiles per split (32, 64 or 128; 32 in grouped launches)
   float scale_log2;
 };
 
 inline int tiles_for_tokens(int64_t tokens) { return static_cast<int>((tokens + kTile - 1) / kTile); }
-inline int max_splits_for(int max_blocks, int block_size) {
+inline int max_splits_for(int max_blocks, int block_size, int partition_tiles = kPartitionTiles) {
   const int tiles = tiles_for_tokens(static_cast<int64_t>(max_blocks) * block_size);
-  return (tiles + kPartitionTiles - 1) / kPartitionTiles;
+  return (tiles + partition_tiles - 1) / partition_tiles;
+}
+
+// Split length T of a plain launch: the longest of 128, 64, 32 tiles for which
+// the grid's upper bound S x Hkv x ceil(tiles of the longest table / T) still
+// reaches kMinSplitUnits CTAs (a few waves of two CTAs on each of 152 SMs).
+constexpr int64_t kMinSplitUnits = 1024;
+inline int partition_tiles_for(int num_seqs, int num_kv_heads, int max_blocks, int block_size) {
+  const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads;
+  for (int t = kMaxPartitionTiles; t > kPartitionTiles; t /= 2)
+    if (rows * max_splits_for(max_blocks, block_size, t) >= kMinSplitUnits) return t;
+  return kPartitionTiles;
 }
 
 // Tiles a sequence shares with its group (0 outside grouped launches) and the
@@ -96,8 +113,8 @@ inline int max_splits_for(int max_blocks, int block_size) {
 __device__ __forceinline__ int shared_tiles_of(const Params& p, int s) {
   return p.seq_group ? __ldg(p.group_shared + __ldg(p.seq_group + s)) / kTile : 0;
 }
-__device__ __forceinline__ int splits_for_tiles(int tiles) {
-  return (tiles + kPartitionTiles - 1) / kPartitionTiles;
+__device__ __forceinline__ int splits_for_tiles(const Params& p, int tiles) {
+  return (tiles + p.partition_tiles - 1) / p.partition_tiles;
 }
 
 template <int BS>
@@ -417,8 +434,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   const int L = clamp_context<BS>(p, s, threadIdx.x == 0 && g == 0 && split == 0);
   const int ntiles = (L + kTile - 1) / kTile;
   const int own_begin = min(shared_tiles_of(p, s), ntiles);
-  const int shared_splits = splits_for_tiles(own_begin);
-  const int nsplit = shared_splits + splits_for_tiles(ntiles - own_begin);
+  const int shared_splits = splits_for_tiles(p, own_begin);
+  const int nsplit = shared_splits + splits_for_tiles(p, ntiles - own_begin);
   if (L == 0) {
     if (split == 0) {
       __half* o = p.out + (static_cast<int64_t>(s) * Hq + h0) * kHeadDim;
@@ -428,9 +445,9 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   }
   if (p.seq_group && split == 0 && threadIdx.x == 0 && ntiles - own_begin > p.own_tiles_cap)
     report(p.dev_err, PKV_DEV_BAD_GROUP);  // more own tokens than the grid covers
-  const int tile_begin = own_begin + split * kPartitionTiles;
+  const int tile_begin = own_begin + split * p.partition_tiles;
   if (tile_begin >= ntiles) return;
-  const int n_here = min(kPartitionTiles, ntiles - tile_begin);
+  const int n_here = min(p.partition_tiles, ntiles - tile_begin);
 
   TileStream<BS> ts;
   ts.init(smem, &tmap_k, &tmap_v, g, p.block_tables + static_cast<int64_t>(s) * p.max_blocks,
@@ -531,9 +548,9 @@ __device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUt
     return;
   }
   const int shared_tiles = shared / kTile;
-  const int tile_begin = split * kPartitionTiles;
+  const int tile_begin = split * p.partition_tiles;
   if (tile_begin >= shared_tiles) return;
-  const int n_here = min(kPartitionTiles, shared_tiles - tile_begin);
+  const int n_here = min(p.partition_tiles, shared_tiles - tile_begin);
 
   // every member must hold the shared tokens through the leader's blocks
   const int32_t* lead = p.block_tables + static_cast<int64_t>(first) * p.max_blocks;

@@ -21,8 +21,8 @@ __global__ void __launch_bounds__(kHeadDim) paged_attention_merge_kernel(const P
   L = L < 0 ? 0 : (L > cap ? cap : L);
   const int ntiles = (L + kTile - 1) / kTile;
   const int own_begin = min(shared_tiles_of(p, s), ntiles);
-  const int shared_splits = splits_for_tiles(own_begin);
-  const int nsplit = shared_splits + splits_for_tiles(ntiles - own_begin);
+  const int shared_splits = splits_for_tiles(p, own_begin);
+  const int nsplit = shared_splits + splits_for_tiles(p, ntiles - own_begin);
   if (nsplit == 0 || (nsplit == 1 && shared_splits == 0)) return;
   const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + h;
   const float* ml = p.part_ml + row * p.max_splits * 2;
@@ -143,7 +143,11 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
                                                     block_size, head_dim);
   if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return PKV_ERR_INVALID_ARG;
-  const int own_splits = max_splits_for(max_blocks_per_seq, block_size);
+  // grouped launches keep 512-token splits (their workspace is sized for them)
+  const int partition =
+      grouped ? kPartitionTiles
+              : partition_tiles_for(num_seqs, num_kv_heads, max_blocks_per_seq, block_size);
+  const int own_splits = max_splits_for(max_blocks_per_seq, block_size, partition);
   const int shared_splits =
       grouped ? (tiles_for_tokens(groups.max_shared_tokens) + kPartitionTiles - 1) /
                     kPartitionTiles
@@ -177,6 +181,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
                     kPartitionTiles * kPartitionTiles;
   p.seq_stride = seq_stride_for(num_seqs);
+  p.partition_tiles = partition;
   p.scale_log2 = scale * 1.4426950408889634f;
 
   CUtensorMap mk, mv;

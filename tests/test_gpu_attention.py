@@ -105,6 +105,53 @@ def test_permutation_of_placement_is_bit_exact(ops):
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
+def split_tiles(S, Hkv, max_blocks, bs=16):
+    """The split length the launch picks: the longest of 128, 64, 32 tiles for
+    which S x Hkv x ceil(table tiles / T) still reaches 1024 CTAs."""
+    tiles = -(-max_blocks * bs // 16)
+    for t in (128, 64):
+        if S * Hkv * -(-tiles // t) >= 1024:
+            return t
+    return 32
+
+
+@pytest.mark.parametrize("S,Hkv,G,T", [(256, 4, 2, 128), (32, 8, 4, 64), (8, 8, 1, 32)])
+@pytest.mark.parametrize("fused", [False, True])
+def test_every_split_length_matches_oracle(ops, S, Hkv, G, T, fused):
+    """Splits of 2048, 1024 and 512 tokens: a few long contexts (cut at every
+    kind of boundary) among many short ones, plain and with the fused write."""
+    rng = np.random.default_rng(S + T)
+    lengths = rng.integers(1, 120, size=S)
+    lengths[:6] = [4096, 2049, 2048, 1025, 513, 3000]
+    lengths = lengths.tolist()
+    q, kc, vc, tables, lens = case(S * 7 + T, lengths, Hkv * G, Hkv)
+    assert split_tiles(S, Hkv, tables.shape[1]) == T
+    scale = 1 / np.sqrt(D)
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    err = ops.new_error_word()
+    if fused:
+        rng2 = np.random.default_rng(T)
+        k_new = wl.host_normal_fp16(rng2, (S, Hkv, D))
+        v_new = wl.host_normal_fp16(rng2, (S, Hkv, D))
+        ops.paged_attention_decode_fused(out, torch.from_numpy(q).cuda(),
+                                         torch.from_numpy(k_new).cuda(),
+                                         torch.from_numpy(v_new).cuda(), dk, dv,
+                                         torch.from_numpy(tables).cuda(),
+                                         torch.from_numpy(lens).cuda(), scale, dev_err=err)
+        slots = np.array([oc.slot(tables[s], int(L) - 1, 16) for s, L in enumerate(lengths)],
+                         np.int64)
+        oc.reshape_and_cache(k_new, v_new, slots, kc, vc)
+    else:
+        ops.paged_attention_decode(out, torch.from_numpy(q).cuda(), dk, dv,
+                                   torch.from_numpy(tables).cuda(),
+                                   torch.from_numpy(lens).cuda(), scale, dev_err=err)
+    assert ops.read_error_word(err) == 0
+    assert_close(out.cpu().numpy(), oa.paged_attention_decode(q, kc, vc, tables, lens, scale))
+    if fused:
+        assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
+
+
 def test_batch_order_does_not_change_any_bit(ops):
     """A sequence's splits depend on its own length only, so reordering the
     batch (sorted by length, then longest first) permutes the output rows bit
