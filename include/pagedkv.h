@@ -179,7 +179,9 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
  *   workspace     at least pkv_paged_attention_grouped_workspace_bytes(...)
  * The new tokens must already be in the cache (pkv_reshape_and_cache).  One
  * kernel launch streams every shared prefix and every sequence's own tiles
- * (the shared units first), a second merges the partials.
+ * (the shared units first), a second merges the partials; both kinds of unit
+ * are cut at the split length pkv_paged_attention_decode would use for the
+ * same sizes.
  */
 int pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_cache,
                                        const void* v_cache, const int32_t* block_tables,

@@ -86,7 +86,7 @@ struct Params {
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
   int seq_stride;     // split grid: row y of the grid is sequence (y * seq_stride) % S
-  int partition_tiles;  // T: tiles per split (32, 64 or 128; 32 in grouped launches)
+  int partition_tiles;  // T: tiles per split (32, 64 or 128)
   float scale_log2;
 };
 

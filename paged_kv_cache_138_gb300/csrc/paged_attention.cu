@@ -12,10 +12,18 @@
 namespace pkv {
 namespace attn {
 
-// Log-sum-exp merge of the splits of one (sequence, query head); 128 threads,
-// one output dim each.  Rows whose only split was written directly are skipped.
-__global__ void __launch_bounds__(kHeadDim) paged_attention_merge_kernel(const Params p) {
-  const int h = blockIdx.x, s = blockIdx.y, d = threadIdx.x;
+// Log-sum-exp merge of the splits of each (sequence, query head) row: one
+// warp per row, kMergeRows rows per CTA; lane i reads split i's (m, l) (32 at
+// a time) for the maximum, then every lane accumulates dims 4 i .. 4 i + 3 of
+// the weighted partials with float4 loads.  Rows whose only split wrote the
+// output directly are skipped.
+constexpr int kMergeRows = 8;
+
+__global__ void __launch_bounds__(kMergeRows * 32) paged_attention_merge_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeRows + (threadIdx.x >> 5);
+  if (row >= static_cast<int64_t>(p.num_seqs) * p.num_q_heads) return;
+  const int s = static_cast<int>(row / p.num_q_heads);
   int L = __ldg(p.context_lens + s);
   const int cap = p.max_blocks * p.block_size;
   L = L < 0 ? 0 : (L > cap ? cap : L);
@@ -24,20 +32,31 @@ __global__ void __launch_bounds__(kHeadDim) paged_attention_merge_kernel(const P
   const int shared_splits = splits_for_tiles(p, own_begin);
   const int nsplit = shared_splits + splits_for_tiles(p, ntiles - own_begin);
   if (nsplit == 0 || (nsplit == 1 && shared_splits == 0)) return;
-  const int64_t row = static_cast<int64_t>(s) * p.num_q_heads + h;
   const float* ml = p.part_ml + row * p.max_splits * 2;
-  const float* po = p.part_o + row * p.max_splits * kHeadDim;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + row * p.max_splits * kHeadDim);
   float M = -INFINITY;
-  for (int i = 0; i < nsplit; ++i) M = fmaxf(M, ml[2 * i]);
-  float num = 0.f, den = 0.f;
+  for (int i = lane; i < nsplit; i += 32) M = fmaxf(M, ml[2 * i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
   if (M != -INFINITY) {
+#pragma unroll 4
     for (int i = 0; i < nsplit; ++i) {
       const float c = exp2_approx(ml[2 * i] - M);
-      num += c * po[i * kHeadDim + d];
+      const float4 v = po[i * (kHeadDim / 4) + lane];
+      num.x += c * v.x;
+      num.y += c * v.y;
+      num.z += c * v.z;
+      num.w += c * v.w;
       den += c * ml[2 * i + 1];
     }
   }
-  p.out[row * kHeadDim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+  __half* o = p.out + row * kHeadDim + 4 * lane;
+  o[0] = __float2half_rn(den > 0.f ? num.x / den : 0.f);
+  o[1] = __float2half_rn(den > 0.f ? num.y / den : 0.f);
+  o[2] = __float2half_rn(den > 0.f ? num.z / den : 0.f);
+  o[3] = __float2half_rn(den > 0.f ? num.w / den : 0.f);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -143,15 +162,12 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
                                                     block_size, head_dim);
   if (need > 0 && (!workspace || workspace_bytes < need)) return PKV_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) & 15) return PKV_ERR_INVALID_ARG;
-  // grouped launches keep 512-token splits (their workspace is sized for them)
+  // split length of this launch (the workspace bound assumes the shortest)
   const int partition =
-      grouped ? kPartitionTiles
-              : partition_tiles_for(num_seqs, num_kv_heads, max_blocks_per_seq, block_size);
+      partition_tiles_for(num_seqs, num_kv_heads, max_blocks_per_seq, block_size);
   const int own_splits = max_splits_for(max_blocks_per_seq, block_size, partition);
   const int shared_splits =
-      grouped ? (tiles_for_tokens(groups.max_shared_tokens) + kPartitionTiles - 1) /
-                    kPartitionTiles
-              : 0;
+      grouped ? (tiles_for_tokens(groups.max_shared_tokens) + partition - 1) / partition : 0;
 
   Params p;
   p.out = static_cast<__half*>(out);
@@ -178,8 +194,8 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.group_first = groups.first;
   p.group_shared = groups.shared;
   p.num_groups = groups.num_groups;
-  p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
-                    kPartitionTiles * kPartitionTiles;
+  p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition *
+                    partition;
   p.seq_stride = seq_stride_for(num_seqs);
   p.partition_tiles = partition;
   p.scale_log2 = scale * 1.4426950408889634f;
@@ -193,8 +209,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   if (grouped) {
     // own units: sequences never run past max_own_tokens beyond their shared
     // prefix (a sequence outside any group counts all its tokens as its own)
-    const int own = (tiles_for_tokens(groups.max_own_tokens) + kPartitionTiles - 1) /
-                    kPartitionTiles;
+    const int own = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition;
     switch (block_size) {
       case 8: rc = launch_grouped_step<8>(G, mk, mv, p, shared_splits, own, st); break;
       case 16: rc = launch_grouped_step<16>(G, mk, mv, p, shared_splits, own, st); break;
@@ -211,7 +226,9 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   }
   if (rc != PKV_OK) return rc;
   if (p.max_splits > 1) {
-    paged_attention_merge_kernel<<<dim3(p.num_q_heads, p.num_seqs), kHeadDim, 0, st>>>(p);
+    const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+    paged_attention_merge_kernel<<<static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows),
+                                   kMergeRows * 32, 0, st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
