@@ -306,7 +306,14 @@ def run_ours(args):
                                           step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
                                           stream=stream)
                 attn_events[k][0].record(stream)
-                if step.groups is not None:
+                if step.groups is not None and step.fused:
+                    gf, sg, gs, mx, mo = step.groups
+                    ops.paged_attention_decode_grouped_fused(
+                        step.out[i], step.q[i], step.k_new[i], step.v_new[i], step.k_cache[i],
+                        step.v_cache[i], step.block_tables, step.context_lens, gf, sg, gs, mx,
+                        mo, step.scale, workspace=step.workspace, dev_err=step.dev_err,
+                        stream=stream)
+                elif step.groups is not None:
                     gf, sg, gs, mx, mo = step.groups
                     ops.paged_attention_decode_grouped(
                         step.out[i], step.q[i], step.k_cache[i], step.v_cache[i],
@@ -410,7 +417,11 @@ def run_ours(args):
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "algorithmic_bytes_per_launch": layer_kv,
-                "kernel": ("paged_attention_decode_fused (cache write + split kernel + LSE "
+                "kernel": ("paged_attention_decode_grouped%s (%sshared-prefix + own-tile "
+                           "units, LSE merge, CUDA events)"
+                           % (("_fused", "cache write + ") if step.fused else ("", ""))
+                           if step.groups is not None else
+                           "paged_attention_decode_fused (cache write + split kernel + LSE "
                            "merge, CUDA events)" if step.fused else
                            "paged_attention_decode (split kernel + LSE merge, CUDA events)"),
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}

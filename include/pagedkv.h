@@ -194,6 +194,25 @@ int pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_c
                                        float scale, void* workspace, size_t workspace_bytes,
                                        int32_t* dev_err, void* stream);
 
+/*
+ * Fused cache write + grouped attention: what pkv_reshape_and_cache of the
+ * step's new tokens followed by pkv_paged_attention_decode_grouped does, in
+ * one launch (as pkv_paged_attention_decode_fused is to
+ * pkv_paged_attention_decode).  The new token of sequence s (position
+ * context_lens[s] - 1, slot from its block table) must lie past its group's
+ * shared prefix, in a block of its own (copy-on-write makes it so); otherwise
+ * the write is skipped and PKV_DEV_BAD_GROUP reported.
+ *   k_new, v_new  fp16 [num_seqs, num_kv_heads, head_dim], 16-byte aligned
+ * Other arguments, layouts and errors as pkv_paged_attention_decode_grouped.
+ */
+int pkv_paged_attention_decode_grouped_fused(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+    void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const int32_t* group_first, const int32_t* seq_group, const int32_t* group_shared,
+    int num_groups, int max_shared_tokens, int max_own_tokens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
+    float scale, void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
+
 /* Workspace bytes pkv_paged_attention_decode_grouped needs (host only). */
 size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads,
                                                    int max_blocks_per_seq, int block_size,
@@ -454,11 +473,13 @@ typedef struct pkv_decode_launch {
 size_t pkv_sched_meta_bytes(const pkv_scheduler* sched);
 
 /* Enqueue the decode part of a planned step on `stream`: copy the batch's
- * slots, block tables, context lengths and groups from out's (pinned) arrays
- * to d->meta, write the new tokens' K/V at their slots, and run paged
- * attention -- grouped when the step planned shared-prefix groups.  The
- * caller has filled q / k_new / v_new for rows 0 .. out->num_batch - 1 and
- * enqueued the step's swaps, prefill writes and copies before. */
+ * block tables, context lengths and groups from out's (pinned) arrays to
+ * d->meta, then one fused launch writes the new tokens' K/V at their slots
+ * (recomputed from the tables; they equal out->slots) and runs paged
+ * attention -- grouped when the step planned shared-prefix groups -- plus
+ * the merge launch when a context spans several splits.  The caller has
+ * filled q / k_new / v_new for rows 0 .. out->num_batch - 1 and enqueued the
+ * step's swaps, prefill writes and copies before. */
 int pkv_sched_launch_decode(const pkv_scheduler* sched, const pkv_sched_step_out* out,
                             const pkv_decode_launch* d, void* stream);
 

@@ -445,6 +445,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   }
   if (p.seq_group && split == 0 && threadIdx.x == 0 && ntiles - own_begin > p.own_tiles_cap)
     report(p.dev_err, PKV_DEV_BAD_GROUP);  // more own tokens than the grid covers
+  // FUSED in a grouped launch: the new token must fall in the sequence's own
+  // tiles (the only ones its own units stream); in a shared tile it would be
+  // a token written into a block its whole group reads
+  if (FUSED && p.seq_group && split == 0 && threadIdx.x == 0 && (L - 1) / kTile < own_begin)
+    report(p.dev_err, PKV_DEV_BAD_GROUP);
   const int tile_begin = own_begin + split * p.partition_tiles;
   if (tile_begin >= ntiles) return;
   const int n_here = min(p.partition_tiles, ntiles - tile_begin);
@@ -469,8 +474,17 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
     for (int kc = 0; kc < 8; ++kc) qa[kc][0] = qa[kc][1] = 0u;
   }
 
-  // the new token (FUSED): its tile, its row within the tile
+  // the new token (FUSED): its tile, its row within the tile; the warp that
+  // will hold that tile loads the token's K (lanes 0-15) / V (16-31) now, so
+  // the load is done by the time the tile lands
   const int new_tile = (L - 1) / kTile, new_row = (L - 1) % kTile;
+  uint4 new_val = make_uint4(0u, 0u, 0u, 0u);
+  if (FUSED && new_tile >= tile_begin && new_tile < tile_begin + n_here &&
+      (new_tile - tile_begin) % kWarps == warp) {
+    const int64_t src =
+        (static_cast<int64_t>(s) * p.num_kv_heads + g) * kHeadDim + (lane & 15) * 8;
+    new_val = *reinterpret_cast<const uint4*>((lane >= 16 ? p.v_new : p.k_new) + src);
+  }
 
   float m = -INFINITY, l = 0.f;
   float o[16][4];
@@ -483,8 +497,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
       const int row_in_block = (L - 1) % BS;
       const int c = lane & 15;
       const bool is_v = lane >= 16;
-      const int64_t src = (static_cast<int64_t>(s) * p.num_kv_heads + g) * kHeadDim + c * 8;
-      const uint4 val = *reinterpret_cast<const uint4*>((is_v ? p.v_new : p.k_new) + src);
+      const uint4 val = new_val;
       const int64_t dst =
           ((static_cast<int64_t>(blk) * BS + row_in_block) * p.num_kv_heads + g) * kHeadDim +
           c * 8;
@@ -648,8 +661,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // One launch for a grouped step, 1-D grid: first the shared-prefix units
 // (KV head, group, shared split) -- the long ones, scheduled first -- then the
-// members' own units (KV head, sequence, own split).
-template <int G, int BS>
+// members' own units (KV head, sequence, own split).  FUSED: the own unit
+// holding a sequence's last tile also writes its new token to the cache.
+template <int G, int BS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_attention_grouped_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    const __grid_constant__ CUtensorMap tmap_v, const Params p,
@@ -665,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     u -= n_shared;
     const int g = u % p.num_kv_heads;
     u /= p.num_kv_heads;
-    split_body<G, BS, false>(tmap_k, tmap_v, p, smem, g, u % p.num_seqs, u / p.num_seqs);
+    split_body<G, BS, FUSED>(tmap_k, tmap_v, p, smem, g, u % p.num_seqs, u / p.num_seqs);
   }
 }
 
@@ -697,19 +711,20 @@ int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, in
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <int G, int BS>
+template <int G, int BS, bool FUSED>
 int launch_grouped(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
                    int shared_splits, int own_splits, cudaStream_t stream) {
   static std::atomic<uint8_t> opted_in[64];
-  const int rc = opt_in_smem(paged_attention_grouped_kernel<G, BS>, opted_in);
+  const int rc = opt_in_smem(paged_attention_grouped_kernel<G, BS, FUSED>, opted_in);
   if (rc != PKV_OK) return rc;
   const int64_t units = static_cast<int64_t>(p.num_kv_heads) *
                         (static_cast<int64_t>(p.num_groups) * shared_splits +
                          static_cast<int64_t>(p.num_seqs) * own_splits);
   if (units <= 0) return PKV_OK;
   if (units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  paged_attention_grouped_kernel<G, BS><<<static_cast<unsigned>(units), kThreads, Smem::alloc,
-                                          stream>>>(mk, mv, p, shared_splits, own_splits);
+  paged_attention_grouped_kernel<G, BS, FUSED>
+      <<<static_cast<unsigned>(units), kThreads, Smem::alloc, stream>>>(mk, mv, p, shared_splits,
+                                                                          own_splits);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -718,13 +733,17 @@ template <int BS>
 int launch_split(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
                  int private_splits, cudaStream_t stream);
 template <int BS>
-int launch_grouped_step(int G, const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-                        int shared_splits, int own_splits, cudaStream_t stream);
+int launch_grouped_step(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const Params& p, int shared_splits, int own_splits, cudaStream_t stream);
 
 #define PKV_CASE_G(GV, BSV)                                                                   \
   case GV:                                                                                    \
     return fused ? launch_one<GV, BSV, true>(mk, mv, p, ps, st)                               \
                  : launch_one<GV, BSV, false>(mk, mv, p, ps, st);
+#define PKV_CASE_GROUPED(GV, BSV)                                                             \
+  case GV:                                                                                    \
+    return fused ? launch_grouped<GV, BSV, true>(mk, mv, p, ss, os, st)                       \
+                 : launch_grouped<GV, BSV, false>(mk, mv, p, ss, os, st);
 #define PKV_DEFINE_LAUNCH_SPLIT(BSV)                                                          \
   template <>                                                                                 \
   int launch_split<BSV>(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv,      \
@@ -738,13 +757,14 @@ int launch_grouped_step(int G, const CUtensorMap& mk, const CUtensorMap& mv, con
     }                                                                                         \
   }                                                                                           \
   template <>                                                                                 \
-  int launch_grouped_step<BSV>(int G, const CUtensorMap& mk, const CUtensorMap& mv,           \
-                               const Params& p, int ss, int os, cudaStream_t st) {            \
+  int launch_grouped_step<BSV>(int G, bool fused, const CUtensorMap& mk,                      \
+                               const CUtensorMap& mv, const Params& p, int ss, int os,        \
+                               cudaStream_t st) {                                             \
     switch (G) {                                                                              \
-      case 1: return launch_grouped<1, BSV>(mk, mv, p, ss, os, st);                           \
-      case 2: return launch_grouped<2, BSV>(mk, mv, p, ss, os, st);                           \
-      case 4: return launch_grouped<4, BSV>(mk, mv, p, ss, os, st);                           \
-      case 8: return launch_grouped<8, BSV>(mk, mv, p, ss, os, st);                           \
+      PKV_CASE_GROUPED(1, BSV)                                                                \
+      PKV_CASE_GROUPED(2, BSV)                                                                \
+      PKV_CASE_GROUPED(4, BSV)                                                                \
+      PKV_CASE_GROUPED(8, BSV)                                                                \
       default: return PKV_ERR_UNSUPPORTED;                                                    \
     }                                                                                         \
   }

@@ -149,7 +149,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   if (grouped) {
     if (!groups.seq_group || !groups.shared || groups.num_groups <= 0 ||
         groups.num_groups > 65535 || groups.max_shared_tokens < 0 ||
-        groups.max_own_tokens < 0 || fused)
+        groups.max_own_tokens < 0)
       return PKV_ERR_INVALID_ARG;
     if (groups.max_shared_tokens % kTile || groups.max_shared_tokens % block_size)
       return PKV_ERR_INVALID_ARG;
@@ -211,10 +211,10 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
     // prefix (a sequence outside any group counts all its tokens as its own)
     const int own = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition;
     switch (block_size) {
-      case 8: rc = launch_grouped_step<8>(G, mk, mv, p, shared_splits, own, st); break;
-      case 16: rc = launch_grouped_step<16>(G, mk, mv, p, shared_splits, own, st); break;
-      case 32: rc = launch_grouped_step<32>(G, mk, mv, p, shared_splits, own, st); break;
-      default: rc = launch_grouped_step<64>(G, mk, mv, p, shared_splits, own, st); break;
+      case 8: rc = launch_grouped_step<8>(G, fused, mk, mv, p, shared_splits, own, st); break;
+      case 16: rc = launch_grouped_step<16>(G, fused, mk, mv, p, shared_splits, own, st); break;
+      case 32: rc = launch_grouped_step<32>(G, fused, mk, mv, p, shared_splits, own, st); break;
+      default: rc = launch_grouped_step<64>(G, fused, mk, mv, p, shared_splits, own, st); break;
     }
   } else {
     switch (block_size) {
@@ -281,6 +281,27 @@ extern "C" int pkv_paged_attention_decode_grouped(
                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                            max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
                            false, gr);
+}
+
+extern "C" int pkv_paged_attention_decode_grouped_fused(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+    void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const int32_t* group_first, const int32_t* seq_group, const int32_t* group_shared,
+    int num_groups, int max_shared_tokens, int max_own_tokens, int num_seqs, int num_q_heads,
+    int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
+    float scale, void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  pkv::attn::Groups gr;
+  gr.first = group_first;
+  gr.seq_group = seq_group;
+  gr.shared = group_shared;
+  gr.num_groups = num_groups;
+  gr.max_shared_tokens = max_shared_tokens;
+  gr.max_own_tokens = max_own_tokens;
+  if (!group_first) return PKV_ERR_INVALID_ARG;
+  return pkv::attn::decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                           num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                           max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
+                           true, gr);
 }
 
 extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,

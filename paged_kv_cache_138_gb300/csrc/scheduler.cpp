@@ -331,9 +331,10 @@ int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
   int32_t* lens = tables + static_cast<size_t>(s->max_batch) * mb;
   int32_t* groups = lens + s->max_batch;  // group_first | seq_group | group_shared
   const bool grouped = o->num_groups > 0 && o->max_shared_tokens > 0;
-  if (cudaMemcpyAsync(slots, o->slots, sizeof(int64_t) * B, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess ||
-      cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb, cudaMemcpyHostToDevice,
+  // the fused launches recompute each new token's slot from its table row, so
+  // the step's slots stay on the host
+  (void)slots;
+  if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb, cudaMemcpyHostToDevice,
                       st) != cudaSuccess ||
       cudaMemcpyAsync(lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
           cudaSuccess)
@@ -350,20 +351,17 @@ int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
                         cudaMemcpyHostToDevice, st) != cudaSuccess)
       return PKV_ERR_CUDA;
   }
-  int rc = pkv_reshape_and_cache(d->k_new, d->v_new, slots, d->k_cache, d->v_cache, B,
-                                 d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks,
-                                 d->dev_err, stream);
-  if (rc != PKV_OK) return rc;
   if (grouped)
-    return pkv_paged_attention_decode_grouped(
-        d->out, d->q, d->k_cache, d->v_cache, tables, lens, gfirst, gseq, gshared,
-        o->num_groups, o->max_shared_tokens, o->max_own_tokens, B, d->num_q_heads,
+    return pkv_paged_attention_decode_grouped_fused(
+        d->out, d->q, d->k_new, d->v_new, d->k_cache, d->v_cache, tables, lens, gfirst, gseq,
+        gshared, o->num_groups, o->max_shared_tokens, o->max_own_tokens, B, d->num_q_heads,
         d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks, mb, d->scale, d->workspace,
         d->workspace_bytes, d->dev_err, stream);
-  return pkv_paged_attention_decode(d->out, d->q, d->k_cache, d->v_cache, tables, lens, B,
-                                    d->num_q_heads, d->num_kv_heads, d->head_dim, s->block_size,
-                                    d->num_blocks, mb, d->scale, d->workspace,
-                                    d->workspace_bytes, d->dev_err, stream);
+  return pkv_paged_attention_decode_fused(d->out, d->q, d->k_new, d->v_new, d->k_cache,
+                                          d->v_cache, tables, lens, B, d->num_q_heads,
+                                          d->num_kv_heads, d->head_dim, s->block_size,
+                                          d->num_blocks, mb, d->scale, d->workspace,
+                                          d->workspace_bytes, d->dev_err, stream);
 }
 
 }  // extern "C"

@@ -24,8 +24,8 @@ class DecodeStep:
         fused: each layer is one launch of the fused cache-write + attention
         kernel instead of reshape_and_cache followed by attention.
         grouped: sequences sharing leading blocks (forked samples) are planned
-        into groups whose shared prefix is streamed once (reshape_and_cache
-        then grouped attention)."""
+        into groups whose shared prefix is streamed once (with fused: one
+        launch writing the new tokens and attending)."""
         self.fused = bool(fused)
         w = batch.workload
         self.batch = batch
@@ -62,7 +62,6 @@ class DecodeStep:
             if mx > 0:
                 self.groups = (torch.from_numpy(gf).to(dev), torch.from_numpy(sg).to(dev),
                                torch.from_numpy(gs).to(dev), mx, mo)
-                self.fused = False
         if self.groups is not None:
             n = ops.grouped_workspace_bytes(S, Hq, batch.max_blocks, self.groups[3], bs)
             self.workspace = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
@@ -84,6 +83,13 @@ class DecodeStep:
         """Layer i of one step.  bufs: the step's input/output tensors (q, k_new,
         v_new, slot_mapping, block_tables, context_lens, out); default self."""
         b = self if bufs is None else bufs
+        if self.fused and self.groups is not None:
+            gf, sg, gs, mx, mo = self.groups
+            ops.paged_attention_decode_grouped_fused(
+                b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
+                b.block_tables, b.context_lens, gf, sg, gs, mx, mo, self.scale,
+                workspace=self.workspace, dev_err=self.dev_err, stream=stream)
+            return
         if self.fused:
             ops.paged_attention_decode_fused(
                 b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
@@ -135,8 +141,8 @@ class DecodeStep:
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
                                          self.batch.max_blocks,
                                          self.batch.workload.block_size) else 0
-        if self.groups is not None:
-            return self.num_layers * 3      # cache write, shared + own tiles, merge
+        if self.groups is not None:         # (cache write,) shared + own tiles, merge
+            return self.num_layers * (2 if self.fused else 3)
         return self.num_layers * ((1 if self.fused else 2) + merge)
 
     def check_errors(self):

@@ -278,3 +278,43 @@ def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, conte
         _stream_handle(stream))
     check(rc, "paged_attention_decode_grouped")
     return out
+
+
+def paged_attention_decode_grouped_fused(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                         context_lens, group_first, seq_group, group_shared,
+                                         max_shared_tokens, max_own_tokens, scale,
+                                         workspace=None, dev_err=None, stream=None):
+    """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
+    sequence (a block past its group's shared prefix) and attend as
+    paged_attention_decode_grouped."""
+    _dev(q, "q", torch.float16, 3)
+    _dev(out, "out", torch.float16, 3)
+    _dev(k_new, "k_new", torch.float16, 3)
+    _dev(v_new, "v_new", torch.float16, 3)
+    _dev(k_cache, "k_cache", torch.float16, 4)
+    _dev(v_cache, "v_cache", torch.float16, 4)
+    _dev(block_tables, "block_tables", torch.int32, 2)
+    _dev(context_lens, "context_lens", torch.int32, 1)
+    for name, t in (("group_first", group_first), ("seq_group", seq_group),
+                    ("group_shared", group_shared)):
+        _dev(t, name, torch.int32, 1)
+    S, Hq, D = q.shape
+    nb, bs, Hkv, _ = k_cache.shape
+    if k_new.shape != (S, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [num_seqs, num_kv_heads, head_dim]")
+    G = group_shared.shape[0]
+    if group_first.shape[0] != G + 1 or seq_group.shape[0] != S:
+        raise ValueError("group arrays do not match")
+    max_blocks = block_tables.shape[1]
+    need = grouped_workspace_bytes(S, Hq, max_blocks, int(max_shared_tokens), bs, D)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib().pkv_paged_attention_decode_grouped_fused(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), _ptr(group_first), _ptr(seq_group),
+        _ptr(group_shared), G, int(max_shared_tokens), int(max_own_tokens), S, Hq, Hkv, D, bs,
+        nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
+        _stream_handle(stream))
+    check(rc, "paged_attention_decode_grouped_fused")
+    return out

@@ -20,9 +20,9 @@ def ops(native_lib):
     return o
 
 
-def forked_case(seed, groups, Hq, Hkv, bs, prefix_tokens, own_max=700):
+def forked_case(seed, groups, Hq, Hkv, bs, prefix_tokens, own_max=700, own_min=0):
     """groups: members per group.  Each group's members share prefix_tokens of
-    blocks, then hold private blocks of 0..own_max further tokens."""
+    blocks, then hold private blocks of own_min..own_max further tokens."""
     rng = np.random.default_rng(seed)
     lens, rows = [], []
     next_block = 0
@@ -31,7 +31,7 @@ def forked_case(seed, groups, Hq, Hkv, bs, prefix_tokens, own_max=700):
         prefix = list(range(next_block, next_block + pb))
         next_block += pb
         for _ in range(members):
-            own = int(rng.integers(0, own_max + 1))
+            own = int(rng.integers(own_min, own_max + 1))
             L = prefix_tokens + own
             extra = -(-L // bs) - pb
             rows.append(prefix + list(range(next_block, next_block + extra)))
@@ -115,3 +115,76 @@ def test_own_tokens_beyond_the_stated_bound_are_reported(ops):
     ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
                                        dev(gf), dev(sg), dev(gs), mx, 100, 0.1, dev_err=err)
     assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
+
+
+def grouped_fused(ops, q, kc, vc, tables, lens, bs, k_new, v_new, err):
+    gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, bs,
+                                                  16 // (q.shape[1] // kc.shape[2]))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    dk, dv = dev(kc), dev(vc)
+    ops.paged_attention_decode_grouped_fused(out, dev(q), dev(k_new), dev(v_new), dk, dv,
+                                             dev(tables), dev(lens), dev(gf), dev(sg), dev(gs),
+                                             mx, mo, 1 / np.sqrt(D), dev_err=err)
+    return out, dk, dv, gs
+
+
+@pytest.mark.parametrize("bs", [8, 16, 64])
+@pytest.mark.parametrize("Hq,Hkv,groups", [(8, 8, [16, 3, 1, 5]), (32, 8, [4, 4, 2, 1])])
+def test_grouped_fused_cache_write_and_attention(ops, bs, Hq, Hkv, groups):
+    """One launch writes every member's new token (in its own blocks) and
+    attends with the shared prefix streamed once: the oracle's cache write
+    then plain attention, and the cache bytes, must agree."""
+    q, kc, vc, tables, lens = forked_case(bs * 3 + Hq, groups, Hq, Hkv, bs, 1024, own_min=1)
+    rng = np.random.default_rng(bs + Hkv)
+    k_new = wl.host_normal_fp16(rng, (len(lens), Hkv, D))
+    v_new = wl.host_normal_fp16(rng, (len(lens), Hkv, D))
+    err = ops.new_error_word()
+    out, dk, dv, gs = grouped_fused(ops, q, kc, vc, tables, lens, bs, k_new, v_new, err)
+    assert ops.read_error_word(err) == 0
+    assert (gs > 0).sum() == sum(1 for m in groups if m > 1)
+    slots = np.array([oc.slot(tables[s], int(L) - 1, bs) for s, L in enumerate(lens)], np.int64)
+    oc.reshape_and_cache(k_new, v_new, slots, kc, vc)
+    ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all() and np.abs(got - ref).max() <= TOL
+    assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
+    assert np.array_equal(dv.cpu().numpy().view(np.uint16), vc.view(np.uint16))
+
+
+def test_grouped_fused_equals_cache_write_then_grouped_bitwise(ops):
+    q, kc, vc, tables, lens = forked_case(77, [8, 5, 1], 32, 8, 16, 1536, own_min=1)
+    rng = np.random.default_rng(78)
+    k_new = wl.host_normal_fp16(rng, (len(lens), 8, D))
+    v_new = wl.host_normal_fp16(rng, (len(lens), 8, D))
+    err = ops.new_error_word()
+    fused, dk, dv, _ = grouped_fused(ops, q, kc, vc, tables, lens, 16, k_new, v_new, err)
+    slots = np.array([oc.slot(tables[s], int(L) - 1, 16) for s, L in enumerate(lens)], np.int64)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    k2, v2 = dev(kc), dev(vc)
+    ops.reshape_and_cache(dev(k_new), dev(v_new), dev(slots), k2, v2)
+    gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, 16, 4)
+    two = torch.empty_like(fused)
+    ops.paged_attention_decode_grouped(two, dev(q), k2, v2, dev(tables), dev(lens), dev(gf),
+                                       dev(sg), dev(gs), mx, mo, 1 / np.sqrt(D), dev_err=err)
+    assert ops.read_error_word(err) == 0
+    assert torch.equal(fused.view(torch.int16), two.view(torch.int16))
+    assert torch.equal(dk.view(torch.int16), k2.view(torch.int16))
+    assert torch.equal(dv.view(torch.int16), v2.view(torch.int16))
+
+
+def test_grouped_fused_new_token_inside_the_shared_prefix_is_reported(ops):
+    """A member whose context ends exactly at the shared prefix would have its
+    new token in a block the group shares: reported, not written there."""
+    q, kc, vc, tables, lens = forked_case(5, [3], 8, 8, 16, 512, own_max=40, own_min=1)
+    lens = lens.copy()
+    lens[1] = 512                                  # member 1 holds only the prefix
+    rng = np.random.default_rng(6)
+    k_new = wl.host_normal_fp16(rng, (3, 8, D))
+    v_new = wl.host_normal_fp16(rng, (3, 8, D))
+    err = ops.new_error_word()
+    _, dk, _, gs = grouped_fused(ops, q, kc, vc, tables, lens, 16, k_new, v_new, err)
+    assert list(gs) == [512]
+    assert ops.read_error_word(err) == 6           # PKV_DEV_BAD_GROUP
+    last = tables[1][511 // 16]
+    assert np.array_equal(dk[last].cpu().numpy().view(np.uint16), kc[last].view(np.uint16))
