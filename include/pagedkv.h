@@ -107,6 +107,15 @@ size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
                                            int max_blocks_per_seq, int block_size,
                                            int head_dim);
 
+/* Split length in tokens (2048, 1024 or 512) that pkv_paged_attention_decode,
+ * _fused and the grouped entry points use for these sizes (host only, no
+ * device call): the longest for which num_seqs x num_kv_heads x
+ * ceil(max_blocks_per_seq * block_size / split) reaches 1024.  A sequence's
+ * output bits are a function of its own data and this split length.
+ * PKV_ERR_INVALID_ARG for non-positive sizes or an unsupported block size. */
+int pkv_paged_attention_split_tokens(int num_seqs, int num_kv_heads, int max_blocks_per_seq,
+                                     int block_size);
+
 /*
  * Fused cache write + attention: one launch does what pkv_reshape_and_cache of
  * the step's new tokens followed by pkv_paged_attention_decode does.  The new

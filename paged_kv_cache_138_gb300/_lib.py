@@ -31,6 +31,7 @@ SIGNATURES = {
     "pkv_paged_attention_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64, _I, _F,
                                         _P, _SZ, _P, _P]),
     "pkv_paged_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "pkv_paged_attention_split_tokens": (_I, [_I, _I, _I, _I]),
     "pkv_paged_attention_decode_grouped": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
                                                 _I, _I, _I, _I, _I64, _I, _F, _P, _SZ, _P, _P]),
     "pkv_paged_attention_grouped_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),

@@ -249,6 +249,15 @@ extern "C" size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_he
   return static_cast<size_t>(num_seqs) * num_q_heads * splits * (kHeadDim + 2) * sizeof(float);
 }
 
+extern "C" int pkv_paged_attention_split_tokens(int num_seqs, int num_kv_heads,
+                                                int max_blocks_per_seq, int block_size) {
+  using namespace pkv::attn;
+  if (num_seqs <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0 ||
+      !supported_block_size(block_size))
+    return PKV_ERR_INVALID_ARG;
+  return partition_tiles_for(num_seqs, num_kv_heads, max_blocks_per_seq, block_size) * kTile;
+}
+
 extern "C" size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads,
                                                               int max_blocks_per_seq,
                                                               int block_size, int head_dim,

@@ -57,6 +57,15 @@ def workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size=BLOCK_
                                                          head_dim))
 
 
+def split_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, block_size=BLOCK_SIZE):
+    """Split length (tokens) the attention launches use for these sizes."""
+    t = lib().pkv_paged_attention_split_tokens(num_seqs, num_kv_heads, max_blocks_per_seq,
+                                               block_size)
+    if t < 0:
+        check(t, "pkv_paged_attention_split_tokens")
+    return t
+
+
 def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None,
                     block_size=BLOCK_SIZE):
     n = workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size)

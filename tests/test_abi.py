@@ -64,3 +64,23 @@ def test_host_side_validation_needs_no_gpu(native_lib):
                                    None) == -1
     assert L.pkv_copy_blocks(None, None, 1, None, 0, 4096, 10, None, None) == 0
     assert L.pkv_copy_blocks(None, None, 1, None, 2, 4095, 10, None, None) == -1
+
+
+def test_split_length_per_launch(native_lib):
+    """The longest split (2048, 1024, 512 tokens) for which S x Hkv x
+    ceil(table tokens / split) still reaches 1024 CTAs."""
+    st = native_lib.pkv_paged_attention_split_tokens
+    assert st(64, 40, 256, 16) == 2048        # the Llama-2-13B layer batch: 5120 CTAs
+    assert st(256, 8, 256, 16) == 2048        # GQA 32/8
+    assert st(64, 32, 256, 16) == 2048        # a Llama-2-7B layer
+    assert st(256, 4, 256, 16) == 2048        # 1024 x 2 CTAs
+    assert st(128, 4, 256, 16) == 2048        # 512 KV rows x 2 splits = 1024
+    assert st(64, 4, 256, 16) == 1024         # 256 x 2 < 1024; 256 x 4 = 1024
+    assert st(32, 8, 256, 16) == 1024         # 256 x 4 = 1024
+    assert st(16, 8, 256, 16) == 512          # 128 x 8 = 1024 (1024-token splits give 512)
+    assert st(8, 8, 256, 16) == 512           # too small for anything longer
+    assert st(1, 1, 4096, 16) == 512          # one 64K-token context: 128 CTAs at best
+    assert st(64, 40, 512, 8) == 2048         # the same tokens in 8-token blocks
+    assert st(64, 40, 64, 64) == 2048
+    assert st(5, 8, 4, 16) == 512             # the tiny batch
+    assert st(0, 8, 4, 16) == -1 and st(4, 8, 4, 12) == -1

@@ -105,14 +105,9 @@ def test_permutation_of_placement_is_bit_exact(ops):
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
 
 
-def split_tiles(S, Hkv, max_blocks, bs=16):
-    """The split length the launch picks: the longest of 128, 64, 32 tiles for
-    which S x Hkv x ceil(table tiles / T) still reaches 1024 CTAs."""
-    tiles = -(-max_blocks * bs // 16)
-    for t in (128, 64):
-        if S * Hkv * -(-tiles // t) >= 1024:
-            return t
-    return 32
+def split_tiles(ops, S, Hkv, max_blocks, bs=16):
+    """The split length (16-token tiles) the launch picks for these sizes."""
+    return ops.split_tokens(S, Hkv, max_blocks, bs) // 16
 
 
 @pytest.mark.parametrize("S,Hkv,G,T", [(256, 4, 2, 128), (32, 8, 4, 64), (8, 8, 1, 32)])
@@ -125,7 +120,7 @@ def test_every_split_length_matches_oracle(ops, S, Hkv, G, T, fused):
     lengths[:6] = [4096, 2049, 2048, 1025, 513, 3000]
     lengths = lengths.tolist()
     q, kc, vc, tables, lens = case(S * 7 + T, lengths, Hkv * G, Hkv)
-    assert split_tiles(S, Hkv, tables.shape[1]) == T
+    assert split_tiles(ops, S, Hkv, tables.shape[1]) == T
     scale = 1 / np.sqrt(D)
     out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
     dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
