@@ -659,18 +659,28 @@ __global__ void __launch_bounds__(kThreads, 2)
   split_body<G, BS, FUSED>(tmap_k, tmap_v, p, aligned_smem(), blockIdx.x, s, blockIdx.z);
 }
 
-// One launch for a grouped step, 1-D grid: first the shared-prefix units
-// (KV head, group, shared split) -- the long ones, scheduled first -- then the
-// members' own units (KV head, sequence, own split).  FUSED: the own unit
-// holding a sequence's last tile also writes its new token to the cache.
+// One launch for a grouped step, 1-D grid of the shared-prefix units (KV
+// head, group, shared split) and the members' own units (KV head, sequence,
+// own split).  The shared units are the long ones and start early: grid
+// positions 0, k, 2k, ... (k = shared_stride) hold them and the own units
+// fill the rest in order.  With k = 1 they all come first; when own units are
+// much shorter than shared ones the host spreads the shared units over the
+// first half of the grid, so that every SM pairs a long unit with short ones
+// instead of running the shared units together and then only short units,
+// whose set-up and drain nothing hides.  FUSED: the own unit holding a
+// sequence's last tile also writes its new token to the cache.
 template <int G, int BS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_attention_grouped_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    const __grid_constant__ CUtensorMap tmap_v, const Params p,
-                                   int shared_splits, int own_splits) {
+                                   int shared_splits, int own_splits, int shared_stride) {
   uint8_t* smem = aligned_smem();
   int u = blockIdx.x;
   const int n_shared = p.num_kv_heads * p.num_groups * shared_splits;
+  if (u % shared_stride == 0 && u / shared_stride < n_shared)
+    u /= shared_stride;  // the (u / k)-th shared unit
+  else
+    u += n_shared - min(n_shared, u / shared_stride + 1);  // own units after the shared ones
   if (u < n_shared) {
     const int g = u % p.num_kv_heads;
     u /= p.num_kv_heads;
@@ -713,7 +723,7 @@ int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, in
 
 template <int G, int BS, bool FUSED>
 int launch_grouped(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p,
-                   int shared_splits, int own_splits, cudaStream_t stream) {
+                   int shared_splits, int own_splits, int shared_stride, cudaStream_t stream) {
   static std::atomic<uint8_t> opted_in[64];
   const int rc = opt_in_smem(paged_attention_grouped_kernel<G, BS, FUSED>, opted_in);
   if (rc != PKV_OK) return rc;
@@ -723,8 +733,8 @@ int launch_grouped(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p
   if (units <= 0) return PKV_OK;
   if (units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   paged_attention_grouped_kernel<G, BS, FUSED>
-      <<<static_cast<unsigned>(units), kThreads, Smem::alloc, stream>>>(mk, mv, p, shared_splits,
-                                                                          own_splits);
+      <<<static_cast<unsigned>(units), kThreads, Smem::alloc, stream>>>(
+          mk, mv, p, shared_splits, own_splits, shared_stride);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -734,7 +744,8 @@ int launch_split(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv
                  int private_splits, cudaStream_t stream);
 template <int BS>
 int launch_grouped_step(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv,
-                        const Params& p, int shared_splits, int own_splits, cudaStream_t stream);
+                        const Params& p, int shared_splits, int own_splits, int shared_stride,
+                        cudaStream_t stream);
 
 #define PKV_CASE_G(GV, BSV)                                                                   \
   case GV:                                                                                    \
@@ -742,8 +753,8 @@ int launch_grouped_step(int G, bool fused, const CUtensorMap& mk, const CUtensor
                  : launch_one<GV, BSV, false>(mk, mv, p, ps, st);
 #define PKV_CASE_GROUPED(GV, BSV)                                                             \
   case GV:                                                                                    \
-    return fused ? launch_grouped<GV, BSV, true>(mk, mv, p, ss, os, st)                       \
-                 : launch_grouped<GV, BSV, false>(mk, mv, p, ss, os, st);
+    return fused ? launch_grouped<GV, BSV, true>(mk, mv, p, ss, os, sk, st)                   \
+                 : launch_grouped<GV, BSV, false>(mk, mv, p, ss, os, sk, st);
 #define PKV_DEFINE_LAUNCH_SPLIT(BSV)                                                          \
   template <>                                                                                 \
   int launch_split<BSV>(int G, bool fused, const CUtensorMap& mk, const CUtensorMap& mv,      \
@@ -759,7 +770,7 @@ int launch_grouped_step(int G, bool fused, const CUtensorMap& mk, const CUtensor
   template <>                                                                                 \
   int launch_grouped_step<BSV>(int G, bool fused, const CUtensorMap& mk,                      \
                                const CUtensorMap& mv, const Params& p, int ss, int os,        \
-                               cudaStream_t st) {                                             \
+                               int sk, cudaStream_t st) {                                     \
     switch (G) {                                                                              \
       PKV_CASE_GROUPED(1, BSV)                                                                \
       PKV_CASE_GROUPED(2, BSV)                                                                \
