@@ -101,8 +101,10 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
                                void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                void* stream);
 
-/* Workspace bytes pkv_paged_attention_decode needs for these sizes (host only;
- * 0 when no sequence can span more than one split of 512 tokens). */
+/* Workspace bytes pkv_paged_attention_decode (and _fused) need for these
+ * sizes (host only): room for the partials of 512-token splits, the shortest
+ * a launch uses, so it covers every split length; 0 when no sequence can span
+ * more than one 512-token split. */
 size_t pkv_paged_attention_workspace_bytes(int num_seqs, int num_q_heads,
                                            int max_blocks_per_seq, int block_size,
                                            int head_dim);

@@ -96,7 +96,7 @@ inline int max_splits_for(int max_blocks, int block_size, int partition_tiles = 
   return (tiles + partition_tiles - 1) / partition_tiles;
 }
 
-// Split length T of a plain launch: the longest of 128, 64, 32 tiles for which
+// Split length T of a launch: the longest of 128, 64, 32 tiles for which
 // the grid's upper bound S x Hkv x ceil(tiles of the longest table / T) still
 // reaches kMinSplitUnits CTAs (a few waves of two CTAs on each of 152 SMs).
 constexpr int64_t kMinSplitUnits = 1024;
