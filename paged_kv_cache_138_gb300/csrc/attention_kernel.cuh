@@ -16,11 +16,14 @@
 //    to fill the GPU with long splits gets short ones.  The G = Hq / Hkv query heads that
 //    read KV head g are handled together, so every K/V byte leaves HBM once.
 //  * Each of the 4 warps streams its own tiles of the split (warp w takes tiles
-//    w, w+4, ...) through a private 3-stage ring in shared memory.  A stage is
+//    w, w+4, ...) through a private 2-stage ring in shared memory.  A stage is
 //    one tile of one KV head: K and V, each as two 64-dim TMA boxes (128-byte
 //    swizzle), 8 KB, completion counted on one mbarrier with a bounded wait.
 //    A tile is a 16-row window of a block (BS >= 16) or two 8-row blocks
 //    (BS = 8); lane 0 refills a stage as soon as the warp is done with it.
+//    Three CTAs share an SM (66 KB of shared memory each): 12 warps x 2 stages
+//    keep 192 KB in flight per SM, and while one CTA sets up or merges the
+//    other two keep streaming.
 //  * Per tile, S = Q K^T and O += P V run on mma.sync m16n8k16 fragments read
 //    with ldmatrix from the swizzled tiles (query heads are the MMA rows).
 //  * Online softmax in base 2 per query row with a lazy rescale: the running
@@ -48,7 +51,8 @@ constexpr int kHeadDim = 128;
 constexpr int kTile = 16;                          // tokens per stage
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
+constexpr int kCtasPerSm = 3;                      // 3 x (4 x 2 x 8 KB rings) per SM
 constexpr int kPartitionTiles = 32;                // shortest split T (512 tokens)
 constexpr int kMaxPartitionTiles = 128;            // longest split: 32 tiles per warp
 constexpr int kHalfTileBytes = kTile * 64 * 2;     // 16 rows x 128 B
@@ -98,7 +102,7 @@ inline int max_splits_for(int max_blocks, int block_size, int partition_tiles = 
 
 // Split length T of a launch: the longest of 128, 64, 32 tiles for which
 // the grid's upper bound S x Hkv x ceil(tiles of the longest table / T) still
-// reaches kMinSplitUnits CTAs (a few waves of two CTAs on each of 152 SMs).
+// reaches kMinSplitUnits CTAs (a few waves of three CTAs on each of 152 SMs).
 constexpr int64_t kMinSplitUnits = 1024;
 inline int partition_tiles_for(int num_seqs, int num_kv_heads, int max_blocks, int block_size) {
   const int64_t rows = static_cast<int64_t>(num_seqs) * num_kv_heads;
@@ -652,7 +656,7 @@ __device__ __forceinline__ uint8_t* aligned_smem() {
 // therefore takes sequence (y * seq_stride) % S, a stride coprime with S
 // near 0.618 S, which spreads neighbours in the batch across the grid.
 template <int G, int BS, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
   const int s = static_cast<int>(static_cast<int64_t>(blockIdx.y) * p.seq_stride % p.num_seqs);
@@ -670,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // whose set-up and drain nothing hides.  FUSED: the own unit holding a
 // sequence's last tile also writes its new token to the cache.
 template <int G, int BS, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_attention_grouped_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    const __grid_constant__ CUtensorMap tmap_v, const Params p,
                                    int shared_splits, int own_splits, int shared_stride) {
