@@ -277,8 +277,6 @@ def run_ours(args):
                                         layers=w.num_layers)
     stream = torch.cuda.current_stream(device)
 
-    from paged_kv_cache_138_gb300 import ops
-
     def one_step():
         step.apply_cow(stream)
         step.run(stream)
@@ -302,34 +300,9 @@ def run_ours(args):
             step.apply_cow(stream)
             for i in range(step.num_layers):
                 if not step.fused:
-                    ops.reshape_and_cache(step.k_new[i], step.v_new[i], step.slot_mapping,
-                                          step.k_cache[i], step.v_cache[i], dev_err=step.dev_err,
-                                          stream=stream)
+                    step.cache_write(i, stream)
                 attn_events[k][0].record(stream)
-                if step.groups is not None and step.fused:
-                    gf, sg, gs, mx, mo = step.groups
-                    ops.paged_attention_decode_grouped_fused(
-                        step.out[i], step.q[i], step.k_new[i], step.v_new[i], step.k_cache[i],
-                        step.v_cache[i], step.block_tables, step.context_lens, gf, sg, gs, mx,
-                        mo, step.scale, workspace=step.workspace, dev_err=step.dev_err,
-                        stream=stream)
-                elif step.groups is not None:
-                    gf, sg, gs, mx, mo = step.groups
-                    ops.paged_attention_decode_grouped(
-                        step.out[i], step.q[i], step.k_cache[i], step.v_cache[i],
-                        step.block_tables, step.context_lens, gf, sg, gs, mx, mo, step.scale,
-                        workspace=step.workspace, dev_err=step.dev_err, stream=stream)
-                elif step.fused:
-                    ops.paged_attention_decode_fused(
-                        step.out[i], step.q[i], step.k_new[i], step.v_new[i], step.k_cache[i],
-                        step.v_cache[i], step.block_tables, step.context_lens, step.scale,
-                        workspace=step.workspace, dev_err=step.dev_err, stream=stream)
-                else:
-                    ops.paged_attention_decode(step.out[i], step.q[i], step.k_cache[i],
-                                               step.v_cache[i], step.block_tables,
-                                               step.context_lens, step.scale,
-                                               workspace=step.workspace, dev_err=step.dev_err,
-                                               stream=stream)
+                step.attend(i, stream)
                 attn_events[k][1].record(stream)
                 k += 1
         stop.record(stream)

@@ -69,6 +69,7 @@ class DecodeStep:
             self.workspace = ops.alloc_workspace(S, Hq, batch.max_blocks, dev, bs)
         self.dev_err = ops.new_error_word(dev)
         self._host = None
+        self._launches = {}   # prepared launches by (kind, layer, stream, buffer set)
 
     # ---- device-resident step ---------------------------------------------------
     def apply_cow(self, stream=None):
@@ -82,32 +83,53 @@ class DecodeStep:
     def run_layer(self, i, stream=None, bufs=None):
         """Layer i of one step.  bufs: the step's input/output tensors (q, k_new,
         v_new, slot_mapping, block_tables, context_lens, out); default self."""
+        if not self.fused:
+            self.cache_write(i, stream, bufs)
+        self.attend(i, stream, bufs)
+
+    def _prepared(self, kind, i, stream, bufs, make):
+        """The launch `kind` of layer i on (stream, bufs), marshalled once."""
+        key = (kind, i, ops._stream_handle(stream).value, id(bufs))
+        launch = self._launches.get(key)
+        if launch is None:
+            launch = self._launches[key] = make()
+        return launch
+
+    def cache_write(self, i, stream=None, bufs=None):
+        """reshape_and_cache of layer i's new tokens (unfused steps)."""
         b = self if bufs is None else bufs
-        if self.fused and self.groups is not None:
-            gf, sg, gs, mx, mo = self.groups
-            ops.paged_attention_decode_grouped_fused(
-                b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
-                b.block_tables, b.context_lens, gf, sg, gs, mx, mo, self.scale,
-                workspace=self.workspace, dev_err=self.dev_err, stream=stream)
-            return
-        if self.fused:
-            ops.paged_attention_decode_fused(
-                b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
-                b.block_tables, b.context_lens, self.scale, workspace=self.workspace,
-                dev_err=self.dev_err, stream=stream)
-            return
-        ops.reshape_and_cache(b.k_new[i], b.v_new[i], b.slot_mapping, self.k_cache[i],
-                              self.v_cache[i], dev_err=self.dev_err, stream=stream)
-        if self.groups is not None:
-            gf, sg, gs, mx, mo = self.groups
-            ops.paged_attention_decode_grouped(
+        self._prepared("write", i, stream, b, lambda: ops.reshape_and_cache(
+            b.k_new[i], b.v_new[i], b.slot_mapping, self.k_cache[i], self.v_cache[i],
+            dev_err=self.dev_err, stream=stream, prepare=True))()
+
+    def attend(self, i, stream=None, bufs=None):
+        """Layer i's attention launch (with the cache write when fused)."""
+        b = self if bufs is None else bufs
+
+        def make():
+            if self.groups is not None:
+                gf, sg, gs, mx, mo = self.groups
+                if self.fused:
+                    return ops.paged_attention_decode_grouped_fused(
+                        b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i],
+                        self.v_cache[i], b.block_tables, b.context_lens, gf, sg, gs, mx, mo,
+                        self.scale, workspace=self.workspace, dev_err=self.dev_err,
+                        stream=stream, prepare=True)
+                return ops.paged_attention_decode_grouped(
+                    b.out[i], b.q[i], self.k_cache[i], self.v_cache[i], b.block_tables,
+                    b.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
+                    dev_err=self.dev_err, stream=stream, prepare=True)
+            if self.fused:
+                return ops.paged_attention_decode_fused(
+                    b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
+                    b.block_tables, b.context_lens, self.scale, workspace=self.workspace,
+                    dev_err=self.dev_err, stream=stream, prepare=True)
+            return ops.paged_attention_decode(
                 b.out[i], b.q[i], self.k_cache[i], self.v_cache[i], b.block_tables,
-                b.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
-                dev_err=self.dev_err, stream=stream)
-            return
-        ops.paged_attention_decode(b.out[i], b.q[i], self.k_cache[i], self.v_cache[i],
-                                   b.block_tables, b.context_lens, self.scale,
-                                   workspace=self.workspace, dev_err=self.dev_err, stream=stream)
+                b.context_lens, self.scale, workspace=self.workspace, dev_err=self.dev_err,
+                stream=stream, prepare=True)
+
+        self._prepared("attend", i, stream, b, make)()
 
     def run(self, stream=None, bufs=None):
         for i in range(self.num_layers):

@@ -39,6 +39,32 @@ def _dev(t, name, dtype, ndim=None):
     return t
 
 
+class PreparedLaunch:
+    """One C-ABI launch whose arguments were checked and marshalled once.
+
+    Calling it enqueues the same launch again: same tensors (their current
+    contents), same stream.  It keeps those tensors alive.  The per-call cost
+    is the C call alone, for loops that relaunch on fixed buffers (the
+    ``prepare=True`` form of the launch functions below)."""
+
+    __slots__ = ("_fn", "_args", "_what", "_keep")
+
+    def __init__(self, fn, args, what, keep):
+        self._fn, self._args, self._what, self._keep = fn, args, what, keep
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != 0:
+            check(rc, self._what)
+
+
+def _issue(fn, args, what, keep, prepare, result):
+    if prepare:
+        return PreparedLaunch(fn, args, what, keep)
+    check(fn(*args), what)
+    return result
+
+
 def new_error_word(device=None):
     """A zeroed device int32 for the kernels' first-error code."""
     return torch.zeros(1, dtype=torch.int32, device=device or torch.cuda.current_device())
@@ -75,8 +101,9 @@ def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None,
 
 
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale,
-                           workspace=None, dev_err=None, stream=None):
-    """out[s,h] = softmax(scale * q[s,h] . K_s^T) V_s over context_lens[s] tokens."""
+                           workspace=None, dev_err=None, stream=None, prepare=False):
+    """out[s,h] = softmax(scale * q[s,h] . K_s^T) V_s over context_lens[s] tokens.
+    prepare=True returns a PreparedLaunch instead of launching."""
     _dev(q, "q", torch.float16, 3)
     _dev(out, "out", torch.float16, 3)
     _dev(k_cache, "k_cache", torch.float16, 4)
@@ -94,18 +121,20 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
     if need and workspace is None:
         workspace = alloc_workspace(S, Hq, max_blocks, q.device, bs)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib().pkv_paged_attention_decode(
-        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        S, Hq, Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes,
-        _ptr(dev_err), _stream_handle(stream))
-    check(rc, "paged_attention_decode")
-    return out
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), S, Hq, Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace),
+            ws_bytes, _ptr(dev_err), _stream_handle(stream))
+    keep = (out, q, k_cache, v_cache, block_tables, context_lens, workspace, dev_err, stream)
+    return _issue(lib().pkv_paged_attention_decode, args, "paged_attention_decode", keep, prepare,
+                  out)
 
 
 def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_tables,
-                                 context_lens, scale, workspace=None, dev_err=None, stream=None):
+                                 context_lens, scale, workspace=None, dev_err=None, stream=None,
+                                 prepare=False):
     """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
-    sequence (slot from its block table) and attend over context_lens[s] tokens."""
+    sequence (slot from its block table) and attend over context_lens[s] tokens.
+    prepare=True returns a PreparedLaunch instead of launching."""
     _dev(q, "q", torch.float16, 3)
     _dev(out, "out", torch.float16, 3)
     _dev(k_new, "k_new", torch.float16, 3)
@@ -125,16 +154,19 @@ def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_t
     if need and workspace is None:
         workspace = alloc_workspace(S, Hq, max_blocks, q.device, bs)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib().pkv_paged_attention_decode_fused(
-        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-        _ptr(block_tables), _ptr(context_lens), S, Hq, Hkv, D, bs, nb, max_blocks, float(scale),
-        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream_handle(stream))
-    check(rc, "paged_attention_decode_fused")
-    return out
+    args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), S, Hq, Hkv, D, bs, nb, max_blocks,
+            float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream_handle(stream))
+    keep = (out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, workspace,
+            dev_err, stream)
+    return _issue(lib().pkv_paged_attention_decode_fused, args, "paged_attention_decode_fused",
+                  keep, prepare, out)
 
 
-def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, dev_err=None, stream=None):
-    """k_cache[slot // bs, slot % bs] = k[i] (and v) for slot = slot_mapping[i] >= 0."""
+def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, dev_err=None, stream=None,
+                      prepare=False):
+    """k_cache[slot // bs, slot % bs] = k[i] (and v) for slot = slot_mapping[i] >= 0.
+    prepare=True returns a PreparedLaunch instead of launching."""
     _dev(k, "k", torch.float16, 3)
     _dev(v, "v", torch.float16, 3)
     _dev(slot_mapping, "slot_mapping", torch.int64, 1)
@@ -146,10 +178,10 @@ def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, dev_err=None, stream
         raise ValueError("shape mismatch")
     if slot_mapping.shape[0] != T:
         raise ValueError("slot_mapping must have one entry per token")
-    rc = lib().pkv_reshape_and_cache(_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache),
-                                     _ptr(v_cache), T, Hkv, D, bs, nb, _ptr(dev_err),
-                                     _stream_handle(stream))
-    check(rc, "reshape_and_cache")
+    args = (_ptr(k), _ptr(v), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), T, Hkv, D, bs,
+            nb, _ptr(dev_err), _stream_handle(stream))
+    keep = (k, v, slot_mapping, k_cache, v_cache, dev_err, stream)
+    return _issue(lib().pkv_reshape_and_cache, args, "reshape_and_cache", keep, prepare, None)
 
 
 def slot_mapping(block_tables, positions, num_blocks, block_size=BLOCK_SIZE, out=None,
@@ -257,9 +289,10 @@ def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_share
 def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, context_lens,
                                    group_first, seq_group, group_shared, max_shared_tokens,
                                    max_own_tokens, scale, workspace=None, dev_err=None,
-                                   stream=None):
+                                   stream=None, prepare=False):
     """Same result as paged_attention_decode; each group's shared prefix is read
-    once for all its members (see shared_prefix_groups)."""
+    once for all its members (see shared_prefix_groups).  prepare=True returns a
+    PreparedLaunch instead of launching."""
     _dev(q, "q", torch.float16, 3)
     _dev(out, "out", torch.float16, 3)
     _dev(k_cache, "k_cache", torch.float16, 4)
@@ -279,20 +312,21 @@ def paged_attention_decode_grouped(out, q, k_cache, v_cache, block_tables, conte
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib().pkv_paged_attention_decode_grouped(
-        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        _ptr(group_first), _ptr(seq_group), _ptr(group_shared), G, int(max_shared_tokens),
-        int(max_own_tokens), S, Hq,
-        Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
-        _stream_handle(stream))
-    check(rc, "paged_attention_decode_grouped")
-    return out
+    args = (_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+            _ptr(context_lens), _ptr(group_first), _ptr(seq_group), _ptr(group_shared), G,
+            int(max_shared_tokens), int(max_own_tokens), S, Hq, Hkv, D, bs, nb, max_blocks,
+            float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream_handle(stream))
+    keep = (out, q, k_cache, v_cache, block_tables, context_lens, group_first, seq_group,
+            group_shared, workspace, dev_err, stream)
+    return _issue(lib().pkv_paged_attention_decode_grouped, args,
+                  "paged_attention_decode_grouped", keep, prepare, out)
 
 
 def paged_attention_decode_grouped_fused(out, q, k_new, v_new, k_cache, v_cache, block_tables,
                                          context_lens, group_first, seq_group, group_shared,
                                          max_shared_tokens, max_own_tokens, scale,
-                                         workspace=None, dev_err=None, stream=None):
+                                         workspace=None, dev_err=None, stream=None,
+                                         prepare=False):
     """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
     sequence (a block past its group's shared prefix) and attend as
     paged_attention_decode_grouped."""
@@ -319,11 +353,12 @@ def paged_attention_decode_grouped_fused(out, q, k_new, v_new, k_cache, v_cache,
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib().pkv_paged_attention_decode_grouped_fused(
-        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-        _ptr(block_tables), _ptr(context_lens), _ptr(group_first), _ptr(seq_group),
-        _ptr(group_shared), G, int(max_shared_tokens), int(max_own_tokens), S, Hq, Hkv, D, bs,
-        nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
-        _stream_handle(stream))
-    check(rc, "paged_attention_decode_grouped_fused")
-    return out
+    args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+            _ptr(block_tables), _ptr(context_lens), _ptr(group_first), _ptr(seq_group),
+            _ptr(group_shared), G, int(max_shared_tokens), int(max_own_tokens), S, Hq, Hkv, D,
+            bs, nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
+            _stream_handle(stream))
+    keep = (out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, group_first,
+            seq_group, group_shared, workspace, dev_err, stream)
+    return _issue(lib().pkv_paged_attention_decode_grouped_fused, args,
+                  "paged_attention_decode_grouped_fused", keep, prepare, out)
