@@ -21,6 +21,10 @@ namespace attn {
 constexpr int kMergeRows = 8;
 
 __global__ void __launch_bounds__(kMergeRows * 32) paged_attention_merge_kernel(const Params p) {
+  // launched as a programmatic dependent of the attention kernel: CTAs may be
+  // resident before it finishes; wait here until its writes are visible (a
+  // no-op for an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeRows + (threadIdx.x >> 5);
   if (row >= static_cast<int64_t>(p.num_seqs) * p.num_q_heads) return;
@@ -240,10 +244,20 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   }
   if (rc != PKV_OK) return rc;
   if (p.max_splits > 1) {
+    // programmatic dependent launch: the merge grid is scheduled while the
+    // attention kernel's last CTAs run and starts the moment it completes
     const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
-    paged_attention_merge_kernel<<<static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows),
-                                   kMergeRows * 32, 0, st>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((rows + kMergeRows - 1) / kMergeRows));
+    cfg.blockDim = dim3(kMergeRows * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, paged_attention_merge_kernel, p) != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
 }
