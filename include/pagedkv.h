@@ -490,7 +490,10 @@ size_t pkv_sched_meta_bytes(const pkv_scheduler* sched);
  * attention -- grouped when the step planned shared-prefix groups -- plus
  * the merge launch when a context spans several splits.  The caller has
  * filled q / k_new / v_new for rows 0 .. out->num_batch - 1 and enqueued the
- * step's swaps, prefill writes and copies before. */
+ * step's swaps, prefill writes and copies before.  When out's block_tables,
+ * context_lens, group_first, seq_group and group_shared lie back to back in
+ * that order (max_batch x max_blocks, max_batch, max_batch + 1, max_batch and
+ * max_batch int32), the metadata goes to the device in one copy. */
 int pkv_sched_launch_decode(const pkv_scheduler* sched, const pkv_sched_step_out* out,
                             const pkv_decode_launch* d, void* stream);
 

@@ -40,6 +40,11 @@ uint64_t block_hash(uint64_t parent, const int32_t* tokens, int n) {
   return h ^ (h >> 31);
 }
 
+template <class V>
+void grow_for_one(V& v) {
+  if (v.size() == v.capacity()) v.reserve(v.capacity() < 8 ? 16 : 2 * v.capacity());
+}
+
 struct Sequence {
   std::vector<int32_t> table;
   std::vector<int32_t> tokens;
@@ -231,9 +236,12 @@ int pkv_bm_append_slot(pkv_block_manager* bm, int64_t seq_id, int32_t token, int
     const bool cow = !boundary && bm->ref[s.table.back()] > 1;
     // (1) a new or private block first: the only step that can fail
     if ((boundary || cow) && bm->num_free() == 0) return PKV_ERR_OUT_OF_BLOCKS;
-    s.table.reserve(s.table.size() + 1);
-    s.tokens.reserve(s.tokens.size() + 1);
-    s.hashes.reserve(s.hashes.size() + 1);
+    // room for one more entry, reserved before anything changes so the
+    // push_backs below cannot throw; grown geometrically (reserve(n) allocates
+    // exactly n, which would copy the vectors on every append)
+    grow_for_one(s.table);
+    grow_for_one(s.tokens);
+    grow_for_one(s.hashes);
     if (boundary) {
       s.table.push_back(bm->take_block());
     } else if (cow) {

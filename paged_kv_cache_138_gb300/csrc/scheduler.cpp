@@ -30,6 +30,7 @@ struct Request {
   int64_t generated = 0;
   int64_t preemptions = 0;
   bool swapped = false;
+  int64_t decoded_step = -1;  // the step that last gave it a decode token
   std::vector<int64_t> host_blocks;  // swap space holding its blocks while swapped out
   bool done() const { return generated >= max_new; }
 };
@@ -54,6 +55,12 @@ struct pkv_scheduler {
   std::vector<int64_t> running;
   std::deque<int64_t> host_free;
   std::vector<int32_t> table_buf;
+  std::vector<int64_t> pending;  // this step's decode candidates (kept to reuse its storage)
+  std::vector<int> order;        // batch order by first block (grouped steps)
+  std::vector<int32_t> first_block;
+  std::vector<int64_t> scratch64;
+  std::vector<int32_t> scratch32;
+  int64_t step_no = 0;
 
   // The token request `rid` "samples" at position `pos` (no model).
   int32_t sample(int64_t rid, int64_t pos) const {
@@ -197,8 +204,9 @@ int pkv_sched_step(pkv_scheduler* s, pkv_sched_step_out* o) {
     // 3. one decode token per running request; on OutOfBlocks the running
     // request with the most generated tokens among those not yet decoded this
     // step is preempted (p1 picks by that count)
-    std::vector<int64_t> pending = s->running;
-    std::unordered_map<int64_t, char> in_batch;
+    std::vector<int64_t>& pending = s->pending;
+    pending.assign(s->running.begin(), s->running.end());
+    const int64_t step_no = ++s->step_no;
     size_t i = 0;
     while (i < pending.size()) {
       Request& r = s->reqs[pending[i]];
@@ -214,15 +222,15 @@ int pkv_sched_step(pkv_scheduler* s, pkv_sched_step_out* o) {
         o->positions[b] = static_cast<int32_t>(pos);
         o->tokens[b] = tok;
         o->slots[b] = slot;
-        in_batch[r.rid] = 1;
+        r.decoded_step = step_no;
         ++i;
         continue;
       }
       if (rc != PKV_ERR_OUT_OF_BLOCKS) return rc;
       int64_t victim = -1, best = -1;
       for (int64_t rid : s->running) {
-        if (in_batch.count(rid)) continue;
         const Request& c = s->reqs[rid];
+        if (c.decoded_step == step_no) continue;  // already decoded this step
         if (c.generated > best) {
           best = c.generated;
           victim = rid;
@@ -264,35 +272,37 @@ int pkv_sched_step(pkv_scheduler* s, pkv_sched_step_out* o) {
     o->num_cow = static_cast<int32_t>(ncow);
     o->num_groups = o->max_shared_tokens = o->max_own_tokens = 0;
     const int B = o->num_batch;
+    const bool grouping = B > 0 && o->group_limit > 0;
+    if (grouping) {
+      // order the batch by first physical block so requests sharing a prompt
+      // (prefix-cache hits) sit together; the per-row arrays are permuted here
+      // and the tables filled in the final order below
+      s->order.resize(static_cast<size_t>(B));
+      s->first_block.resize(static_cast<size_t>(B));
+      for (int b = 0; b < B; ++b) {
+        int32_t first = -1;
+        pkv_bm_block_table(s->bm, o->batch_rids[b], &first, 1);
+        s->first_block[b] = first;
+        s->order[b] = b;
+      }
+      std::stable_sort(s->order.begin(), s->order.end(),
+                       [&](int x, int y) { return s->first_block[x] < s->first_block[y]; });
+      auto permute = [&](auto* a, auto& tmp) {
+        tmp.assign(a, a + B);
+        for (int b = 0; b < B; ++b) a[b] = tmp[s->order[b]];
+      };
+      permute(o->batch_rids, s->scratch64);
+      permute(o->slots, s->scratch64);
+      permute(o->positions, s->scratch32);
+      permute(o->tokens, s->scratch32);
+    }
     if (B > 0) {
       const int rc = pkv_bm_fill_block_tables(s->bm, o->batch_rids, B, o->block_tables,
                                               s->max_blocks, -1, o->context_lens);
       if (rc != PKV_OK) return rc;
     }
-    if (B > 0 && o->group_limit > 0) {
-      // order the batch by first physical block so requests sharing a prompt
-      // (prefix-cache hits) sit together, then plan their groups
+    if (grouping) {
       const int mb = s->max_blocks;
-      std::vector<int> order(static_cast<size_t>(B));
-      for (int b = 0; b < B; ++b) order[b] = b;
-      std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-        return o->block_tables[static_cast<int64_t>(x) * mb] <
-               o->block_tables[static_cast<int64_t>(y) * mb];
-      });
-      std::vector<int64_t> rids(o->batch_rids, o->batch_rids + B), slots(o->slots, o->slots + B);
-      std::vector<int32_t> pos(o->positions, o->positions + B), toks(o->tokens, o->tokens + B),
-          lens(o->context_lens, o->context_lens + B),
-          tabs(o->block_tables, o->block_tables + static_cast<int64_t>(B) * mb);
-      for (int b = 0; b < B; ++b) {
-        const int src = order[b];
-        o->batch_rids[b] = rids[src];
-        o->slots[b] = slots[src];
-        o->positions[b] = pos[src];
-        o->tokens[b] = toks[src];
-        o->context_lens[b] = lens[src];
-        std::memcpy(o->block_tables + static_cast<int64_t>(b) * mb,
-                    tabs.data() + static_cast<int64_t>(src) * mb, sizeof(int32_t) * mb);
-      }
       if (!o->group_first || !o->seq_group || !o->group_shared) return PKV_ERR_INVALID_ARG;
       int ng = 0, ms = 0, mo = 0;
       const int rc = pkv_plan_shared_prefix_groups(o->block_tables, o->context_lens, B, mb,
@@ -334,15 +344,26 @@ int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
   // the fused launches recompute each new token's slot from its table row, so
   // the step's slots stay on the host
   (void)slots;
-  if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb, cudaMemcpyHostToDevice,
-                      st) != cudaSuccess ||
-      cudaMemcpyAsync(lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
-          cudaSuccess)
-    return PKV_ERR_CUDA;
   int32_t* gfirst = groups;
   int32_t* gseq = groups + s->max_batch + 1;
   int32_t* gshared = gseq + s->max_batch;
-  if (grouped) {
+  // host arrays laid out like the staging area (tables | lens | groups): one copy
+  const size_t MB = static_cast<size_t>(s->max_batch);
+  const bool packed = o->context_lens == o->block_tables + MB * mb &&
+                      o->group_first == o->context_lens + MB &&
+                      o->seq_group == o->group_first + MB + 1 && o->group_shared == o->seq_group + MB;
+  if (packed) {
+    const size_t n = grouped ? MB * mb + MB + 3 * MB + 1 : MB * mb + MB;
+    if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return PKV_ERR_CUDA;
+  } else if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb,
+                             cudaMemcpyHostToDevice, st) != cudaSuccess ||
+             cudaMemcpyAsync(lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
+                             st) != cudaSuccess) {
+    return PKV_ERR_CUDA;
+  }
+  if (grouped && !packed) {
     if (cudaMemcpyAsync(gfirst, o->group_first, sizeof(int32_t) * (o->num_groups + 1),
                         cudaMemcpyHostToDevice, st) != cudaSuccess ||
         cudaMemcpyAsync(gseq, o->seq_group, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=

@@ -100,9 +100,18 @@ class NativeServingDriver:
             "cow_pairs": ((B, 2), torch.int64),
             "groups": ((3 * B + 1,), torch.int32),   # group_first | seq_group | group_shared
         }
+        # block tables, context lengths and groups sit in one pinned buffer in
+        # the layout of the device staging area, so the decode launch moves
+        # them with one copy
+        packed = ("block_tables", "context_lens", "groups")
         self.sets = []
         for _ in range(2):
-            t = {n: torch.zeros(shape, dtype=dt, pin_memory=pin) for n, (shape, dt) in spec.items()}
+            t = {n: torch.zeros(shape, dtype=dt, pin_memory=pin) for n, (shape, dt) in spec.items()
+                 if n not in packed}
+            meta_host = torch.zeros(B * mb + B + 3 * B + 1, dtype=torch.int32, pin_memory=pin)
+            t["block_tables"] = meta_host[:B * mb].view(B, mb)
+            t["context_lens"] = meta_host[B * mb:B * mb + B]
+            t["groups"] = meta_host[B * mb + B:]
             o = _StepOut()
             for name, ten in t.items():
                 if name != "groups":
@@ -119,10 +128,13 @@ class NativeServingDriver:
             self.sets.append({"t": t, "a": {n: x.numpy() for n, x in t.items()}, "out": o,
                               "event": ev, "used": False})
         self.out = torch.empty((B, num_q_heads, head_dim), dtype=torch.float16, device=self.dev)
-        self.k_new = torch.empty((B, num_kv_heads, head_dim), dtype=torch.float16,
-                                 device=self.dev)
-        self.v_new = torch.empty_like(self.k_new)
-        self.q = torch.empty_like(self.out)
+        # the step's q, k_new and v_new: views of one buffer (one generator
+        # launch fills all three)
+        nq, nk = B * num_q_heads * head_dim, B * num_kv_heads * head_dim
+        self.qkv = torch.empty(nq + 2 * nk, dtype=torch.float16, device=self.dev)
+        self.q = self.qkv[:nq].view(B, num_q_heads, head_dim)
+        self.k_new = self.qkv[nq:nq + nk].view(B, num_kv_heads, head_dim)
+        self.v_new = self.qkv[nq + nk:].view(B, num_kv_heads, head_dim)
         self.grouped = bool(grouped)
         if self.grouped:
             # steps without a shared prefix run the plain entry point on the same buffer
@@ -256,11 +268,15 @@ class DeviceRandomValues:
         self.dev = device
 
     def prefill(self, drv, rids, positions):
-        x = torch.randn((2, len(rids), self.Hkv, self.D), generator=self.gen,
-                        device=self.dev).half()
+        x = torch.empty((2, len(rids), self.Hkv, self.D), dtype=torch.float16, device=self.dev)
+        x.normal_(generator=self.gen)
         return x[0], x[1]
 
     def decode_into(self, drv, rids, positions, k, v, q):
+        qkv = getattr(drv, "qkv", None)
+        if qkv is not None:          # the driver's q/k_new/v_new share one buffer
+            qkv.normal_(generator=self.gen)
+            return
         for t in (k, v, q):
             t.normal_(generator=self.gen)
 
