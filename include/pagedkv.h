@@ -332,6 +332,18 @@ int pkv_swap_blocks(const void* const* src_pools, void* const* dst_pools, int nu
  */
 int pkv_selftest_bounded_wait(int32_t* dev_err, int32_t* landed, int limit_ms, void* stream);
 
+/*
+ * Synthetic inputs (benchmarks, the model-less serving driver; not part of the
+ * paged-attention method).  Writes n standard-normal fp16 values to dst (device,
+ * 16-byte aligned): element i is element offset + i of a stream keyed by seed,
+ * so consecutive calls with offsets advancing by n continue one stream.
+ * Element j takes output j / 2 of SplitMix64 (Steele, Lea and Flood 2014)
+ * started at state seed, and the Box-Muller transform of its bits 40..63
+ * (u1 in (0, 1]) and 16..39 (u2 in [0, 1)): cosine for even j, sine for odd.
+ * Returns INVALID_ARG for n < 0 or a misaligned / NULL dst (n > 0).
+ */
+int pkv_fill_normal_f16(void* dst, int64_t n, uint64_t seed, uint64_t offset, void* stream);
+
 /* ---- host BlockManager ---------------------------------------------------- */
 /*
  * The BlockManager of "P06 BlockManager" (free list taken FIFO, reference

@@ -47,6 +47,7 @@ SIGNATURES = {
     "pkv_slot_mapping": (_I, [_P, _P, _I, _I, _I, _I64, _P, _P, _P]),
     "pkv_copy_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _P, _P]),
     "pkv_selftest_bounded_wait": (_I, [_P, _P, _I, _P]),
+    "pkv_fill_normal_f16": (_I, [_P, _I64, ctypes.c_uint64, ctypes.c_uint64, _P]),
     "pkv_swap_blocks": (_I, [_P, _P, _I, _P, _I, _I64, _I64, _I64, _P, _P]),
     "pkv_sched_create": (_P, [_P, _I, _I, _I, _I, _I64, ctypes.c_uint64, _I]),
     "pkv_sched_destroy": (None, [_P]),

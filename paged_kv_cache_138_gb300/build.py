@@ -16,7 +16,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpagedkv.so")
 
 SOURCES = ["attention_bs16.cu", "attention_bs8.cu", "attention_bs32.cu", "attention_bs64.cu",
-           "paged_attention.cu", "cache_ops.cu", "block_manager.cpp", "scheduler.cpp", "api.cpp"]
+           "paged_attention.cu", "cache_ops.cu", "synthetic.cu", "block_manager.cpp",
+           "scheduler.cpp", "api.cpp"]
 HEADERS = [os.path.join(CSRC, "pkv_device.cuh"), os.path.join(CSRC, "attention_kernel.cuh"),
            os.path.join(INCLUDE, "pagedkv.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -65,6 +65,18 @@ def _issue(fn, args, what, keep, prepare, result):
     return result
 
 
+def fill_normal(t, seed, offset, stream=None):
+    """Fill fp16 tensor ``t`` (contiguous, 16-byte aligned) with standard-normal
+    values: elements offset .. offset + numel - 1 of the device stream keyed by
+    ``seed`` (``pkv_fill_normal_f16``).  Returns the offset after them."""
+    _dev(t, "t", torch.float16)
+    n = t.numel()
+    check(lib().pkv_fill_normal_f16(_ptr(t), n, ctypes.c_uint64(seed & 0xFFFFFFFFFFFFFFFF),
+                                    ctypes.c_uint64(offset), _stream_handle(stream)),
+          "pkv_fill_normal_f16")
+    return offset + n
+
+
 def new_error_word(device=None):
     """A zeroed device int32 for the kernels' first-error code."""
     return torch.zeros(1, dtype=torch.int32, device=device or torch.cuda.current_device())

@@ -210,21 +210,25 @@ class NativeServingDriver:
         rc = lib().pkv_sched_step(self._h, ctypes.byref(o))
         if rc != PKV_OK:
             raise PagedKVError(rc, "sched_step")
+        cuda = self.dev.type == "cuda"
+        # one stream for the whole step, looked up once
+        stream = torch.cuda.current_stream(self.dev) if cuda else None
         caches = ([self.k_cache, self.v_cache], [self.host_k, self.host_v])
         if o.num_swap_in:
             ops.swap_blocks(caches[1], caches[0], self._h2d(t["swap_in_pairs"][:o.num_swap_in]),
-                            dev_err=self.dev_err)
+                            dev_err=self.dev_err, stream=stream)
         if o.num_prefill:
             n = o.num_prefill
-            k, v = self.values.prefill(self, a["prefill_rids"][:n], a["prefill_positions"][:n])
+            k, v = self.values.prefill(self, a["prefill_rids"][:n], a["prefill_positions"][:n],
+                                       stream=stream)
             ops.reshape_and_cache(k, v, self._h2d(t["prefill_slots"][:n]), self.k_cache,
-                                  self.v_cache, dev_err=self.dev_err)
+                                  self.v_cache, dev_err=self.dev_err, stream=stream)
         if o.num_swap_out:
             ops.swap_blocks(caches[0], caches[1], self._h2d(t["swap_out_pairs"][:o.num_swap_out]),
-                            dev_err=self.dev_err)
+                            dev_err=self.dev_err, stream=stream)
         if o.num_cow:
             ops.copy_blocks(self.k_cache, self.v_cache, self._h2d(t["cow_pairs"][:o.num_cow]),
-                            dev_err=self.dev_err)
+                            dev_err=self.dev_err, stream=stream)
         B = o.num_batch
         res = {"rids": a["batch_rids"][:B].copy(), "positions": a["positions"][:B].copy(),
                "out": self.out[:B], "admitted": o.num_admitted, "finished": o.num_finished,
@@ -233,12 +237,10 @@ class NativeServingDriver:
                "swap_out": o.num_swap_out, "kv_tokens": int(a["context_lens"][:B].sum()),
                "groups": 0, "shared_tokens": 0}
         if B:
-            self.values.decode_into(self, res["rids"], res["positions"], self.k_new[:B],
-                                    self.v_new[:B], self.q[:B])
+            self.values.decode_into(self, res["rids"], res["positions"], B, stream=stream)
             rc = lib().pkv_sched_launch_decode(
                 self._h, ctypes.byref(o), ctypes.byref(self.launch),
-                ctypes.c_void_p(torch.cuda.current_stream(self.dev).cuda_stream)
-                if self.dev.type == "cuda" else None)
+                ctypes.c_void_p(stream.cuda_stream) if cuda else None)
             if rc != PKV_OK:
                 raise PagedKVError(rc, "sched_launch_decode")
             if o.num_groups and o.max_shared_tokens > 0:
@@ -247,7 +249,7 @@ class NativeServingDriver:
                 res["shared_tokens"] = int(g[2 * self.max_batch + 1:][
                     g[self.max_batch + 1:self.max_batch + 1 + B]].sum())
         if st["event"] is not None:
-            st["event"].record()
+            st["event"].record(stream)
         st["used"] = True
         self.steps += 1
         return res
@@ -259,26 +261,24 @@ class NativeServingDriver:
 
 
 class DeviceRandomValues:
-    """K/V/q drawn on the device (one generator launch per kind per step)."""
+    """K/V/q drawn on the device from one counter-based stream
+    (``ops.fill_normal``): one launch for a step's q, k_new and v_new, one for
+    a step's prefill rows."""
 
     def __init__(self, seed, num_q_heads, num_kv_heads, head_dim=128, device="cuda"):
         self.Hq, self.Hkv, self.D = num_q_heads, num_kv_heads, head_dim
-        self.gen = torch.Generator(device=device)
-        self.gen.manual_seed(seed)
+        self.seed, self.offset = int(seed), 0
         self.dev = device
 
-    def prefill(self, drv, rids, positions):
+    def prefill(self, drv, rids, positions, stream=None):
         x = torch.empty((2, len(rids), self.Hkv, self.D), dtype=torch.float16, device=self.dev)
-        x.normal_(generator=self.gen)
+        self.offset = ops.fill_normal(x, self.seed, self.offset, stream)
         return x[0], x[1]
 
-    def decode_into(self, drv, rids, positions, k, v, q):
-        qkv = getattr(drv, "qkv", None)
-        if qkv is not None:          # the driver's q/k_new/v_new share one buffer
-            qkv.normal_(generator=self.gen)
-            return
-        for t in (k, v, q):
-            t.normal_(generator=self.gen)
+    def decode_into(self, drv, rids, positions, num_rows, stream=None):
+        """Fill rows 0 .. num_rows - 1 of the driver's q, k_new and v_new (the
+        three share one buffer, so the whole buffer is drawn in one launch)."""
+        self.offset = ops.fill_normal(drv.qkv, self.seed, self.offset, stream)
 
 
 class ContentKeyedValues:
@@ -300,13 +300,13 @@ class ContentKeyedValues:
         return (torch.from_numpy(np.stack(ks)).to(self.dev),
                 torch.from_numpy(np.stack(vs)).to(self.dev))
 
-    def prefill(self, drv, rids, positions):
+    def prefill(self, drv, rids, positions, stream=None):
         return self._kv(drv, rids, positions)
 
-    def decode_into(self, drv, rids, positions, k_out, v_out, q_out):
+    def decode_into(self, drv, rids, positions, num_rows, stream=None):
         k, v = self._kv(drv, rids, positions)
         q = np.stack([wl.step_query_host(self.seed, r, p, self.Hq, self.D)
                       for r, p in zip(rids.tolist(), positions.tolist())])
-        k_out.copy_(k)
-        v_out.copy_(v)
-        q_out.copy_(torch.from_numpy(q))
+        drv.k_new[:num_rows].copy_(k)
+        drv.v_new[:num_rows].copy_(v)
+        drv.q[:num_rows].copy_(torch.from_numpy(q))
