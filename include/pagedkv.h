@@ -339,7 +339,9 @@ int pkv_selftest_bounded_wait(int32_t* dev_err, int32_t* landed, int limit_ms, v
  * so consecutive calls with offsets advancing by n continue one stream.
  * Element j takes output j / 2 of SplitMix64 (Steele, Lea and Flood 2014)
  * started at state seed, and the Box-Muller transform of its bits 40..63
- * (u1 in (0, 1]) and 16..39 (u2 in [0, 1)): cosine for even j, sine for odd.
+ * (u1 in (0, 1]) and 16..39 (u2 in [0, 1)): cosine for even j, sine for odd,
+ * in fp32 with the hardware sine/cosine (within ~1e-5 of the exact transform
+ * before the fp16 rounding).
  * Returns INVALID_ARG for n < 0 or a misaligned / NULL dst (n > 0).
  */
 int pkv_fill_normal_f16(void* dst, int64_t n, uint64_t seed, uint64_t offset, void* stream);

@@ -11,6 +11,7 @@
 // in (0, 1] and u2 = bits 16..39 / 2^24 in [0, 1), and applies the Box-Muller
 // transform (Box and Muller, 1958): r = sqrt(-2 ln u1), element 2p gets
 // r cos(2 pi u2) and element 2p + 1 gets r sin(2 pi u2), rounded to fp16.
+// A thread draws each pair once and stores 8 values with one 16-byte store.
 #include <algorithm>
 
 #include <cuda_fp16.h>
@@ -32,14 +33,22 @@ __device__ __forceinline__ uint64_t splitmix64_output(uint64_t seed, uint64_t p)
   return z ^ (z >> 31);
 }
 
-__device__ __forceinline__ float normal_at(uint64_t seed, uint64_t j) {
-  const uint64_t w = splitmix64_output(seed, j >> 1);
+// Both values of pair p.  The angle is taken as 2 pi u2 - pi, inside the
+// interval where the hardware sine/cosine is accurate to ~2^-21 absolute, and
+// the signs flipped back: cos(t + pi) = -cos t, sin(t + pi) = -sin t.
+__device__ __forceinline__ float2 normal_pair(uint64_t seed, uint64_t p) {
+  const uint64_t w = splitmix64_output(seed, p);
   const float u1 = static_cast<float>((w >> 40) + 1) * (1.0f / 16777216.0f);
   const float u2 = static_cast<float>((w >> 16) & 0xFFFFFFull) * (1.0f / 16777216.0f);
-  const float r = sqrtf(-2.0f * logf(u1));
+  const float r = sqrtf(-2.0f * logf(u1));   // logf(u1) <= 0 for u1 <= 1
   float s, c;
-  sincospif(2.0f * u2, &s, &c);
-  return r * ((j & 1) ? s : c);
+  __sincosf(6.28318530718f * u2 - 3.14159265359f, &s, &c);
+  return make_float2(-r * c, -r * s);
+}
+
+__device__ __forceinline__ float normal_at(uint64_t seed, uint64_t j) {
+  const float2 v = normal_pair(seed, j >> 1);
+  return (j & 1) ? v.y : v.x;
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -48,10 +57,17 @@ __global__ void __launch_bounds__(kThreads)
   for (int64_t base = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * kPerThread;
        base < n; base += stride) {
     if (base + kPerThread <= n) {
-      __align__(16) __half h[kPerThread];
+      __align__(16) __half2 h[kPerThread / 2];
+      if ((offset & 1) == 0) {         // the thread's elements are whole pairs
+        const uint64_t p0 = (offset + base) >> 1;
 #pragma unroll
-      for (int e = 0; e < kPerThread; ++e)
-        h[e] = __float2half_rn(normal_at(seed, offset + base + e));
+        for (int e = 0; e < kPerThread / 2; ++e) h[e] = __float22half2_rn(normal_pair(seed, p0 + e));
+      } else {
+#pragma unroll
+        for (int e = 0; e < kPerThread / 2; ++e)
+          h[e] = __floats2half2_rn(normal_at(seed, offset + base + 2 * e),
+                                   normal_at(seed, offset + base + 2 * e + 1));
+      }
       *reinterpret_cast<uint4*>(dst + base) = *reinterpret_cast<const uint4*>(h);
     } else {
       for (int64_t e = base; e < n; ++e) dst[e] = __float2half_rn(normal_at(seed, offset + e));

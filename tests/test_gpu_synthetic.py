@@ -37,8 +37,10 @@ def test_matches_host_restatement(native_lib, n, offset):
     seed = 0xC0FFEE
     dev = fill(n, seed, offset).cpu().numpy().astype(np.float64)
     host = host_normals(seed, offset, n)
-    # fp32 Box-Muller rounded to fp16 vs float64: at most one fp16 unit apart
-    tol = np.maximum(np.abs(host), 2.0 ** -14) * 2.0 ** -10 + 2.0 ** -24
+    # fp32 Box-Muller (hardware sine/cosine: ~2^-21 absolute, times r < 5.8,
+    # plus the fp32 angle's rounding) rounded to fp16, against float64: one
+    # fp16 unit apart plus 1e-5
+    tol = np.maximum(np.abs(host), 2.0 ** -14) * 2.0 ** -10 + 1e-5
     assert np.all(np.abs(dev - host) <= tol)
 
 
