@@ -64,3 +64,49 @@ def test_native_serving_matches_oracle_every_step(native_lib, preemption, groupe
         assert stats["shared_tokens"] > 0
     drv.bm.check_invariants()
     assert drv.bm.num_free_blocks == nb
+
+
+@pytest.mark.parametrize("grouped", [False, True])
+def test_native_serving_with_device_values_matches_oracle(native_lib, grouped):
+    """The configuration the serving benchmark times (values drawn on the
+    device, GQA, shared system prompts): every few steps each decoded row is
+    recomputed by the oracle from the cache as the step left it, the step's
+    q rows and the request's block table."""
+    import torch
+    from paged_kv_cache_138_gb300.serving import DeviceRandomValues, NativeServingDriver
+    hq, hkv = 8, 2
+    reqs = wl.serving_requests(SEED + 1, num_requests=24, num_system_prompts=2,
+                               system_prompt_len=48, suffix_max=12, new_min=3, new_max=40)
+    nb, mb = 64, 8
+    drv = NativeServingDriver(nb, hq, hkv, max_batch=8, max_blocks_per_seq=mb,
+                              values=DeviceRandomValues(3, hq, hkv, device="cuda"),
+                              free_order=np.random.default_rng(4).permutation(nb), seed=SEED,
+                              grouped=grouped)
+    for r in reqs:
+        drv.add_request(r.rid, r.prompt, r.max_new_tokens)
+    worst, rows, steps, shared = 0.0, 0, 0, 0
+    while not drv.idle:
+        res = drv.step()
+        steps += 1
+        assert steps < 500
+        shared += res["shared_tokens"]
+        B = len(res["rids"])
+        if B == 0 or steps % 3:
+            continue
+        torch.cuda.synchronize()
+        out = res["out"].cpu().numpy().astype(np.float64)
+        q = drv.q[:B].cpu().numpy()
+        kc, vc = drv.k_cache.cpu().numpy(), drv.v_cache.cpu().numpy()
+        tables = np.full((B, mb), -1, np.int32)
+        for i, rid in enumerate(res["rids"].tolist()):
+            t = drv.bm.block_table(rid)
+            tables[i, :len(t)] = t
+        lens = (res["positions"] + 1).astype(np.int32)
+        ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
+        worst = max(worst, float(np.abs(out - ref).max()))
+        rows += B
+    drv.check_errors()
+    assert rows > 0 and worst <= attention_tolerance(), worst
+    if grouped:
+        assert shared > 0
+    drv.bm.check_invariants()
