@@ -89,6 +89,7 @@ struct Params {
   int64_t num_blocks;
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
+  int shared_splits_cap;  // grouped launches: split slots reserved for a shared prefix
   int seq_stride;     // split grid: row y of the grid is sequence (y * seq_stride) % S
   int partition_tiles;  // T: tiles per split (32, 64 or 128)
   float scale_log2;
@@ -112,13 +113,24 @@ inline int partition_tiles_for(int num_seqs, int num_kv_heads, int max_blocks, i
 }
 
 // Tiles a sequence shares with its group (0 outside grouped launches) and the
-// split slots those take in the workspace.  The shared part always ends on a
-// tile boundary (the host checks group_shared % 16 == 0).
+// split slots those take in the workspace.  The shared part ends on a tile
+// boundary (a group whose shared length is not a multiple of 16 is reported by
+// its shared units).  A group id out of range counts as no shared prefix; the
+// sequence's own units report it.
 __device__ __forceinline__ int shared_tiles_of(const Params& p, int s) {
-  return p.seq_group ? __ldg(p.group_shared + __ldg(p.seq_group + s)) / kTile : 0;
+  if (!p.seq_group) return 0;
+  const int grp = __ldg(p.seq_group + s);
+  if (grp < 0 || grp >= p.num_groups) return 0;
+  return max(__ldg(p.group_shared + grp), 0) / kTile;
 }
 __device__ __forceinline__ int splits_for_tiles(const Params& p, int tiles) {
   return (tiles + p.partition_tiles - 1) / p.partition_tiles;
+}
+// Workspace slots of a sequence's shared prefix: one per split of it, never
+// more than the launch reserved (a group sharing more tokens than the launch
+// was sized for is reported; its rows then stay inside their own slots).
+__device__ __forceinline__ int shared_slots_of(const Params& p, int shared_tiles) {
+  return min(splits_for_tiles(p, shared_tiles), p.shared_splits_cap);
 }
 
 template <int BS>
@@ -435,10 +447,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   const int Hq = p.num_q_heads;
   const int h0 = g * G;
 
+  // the group's shared length first: its two dependent loads then overlap the
+  // context length's
+  const int shared_tiles = shared_tiles_of(p, s);
   const int L = clamp_context<BS>(p, s, threadIdx.x == 0 && g == 0 && split == 0);
   const int ntiles = (L + kTile - 1) / kTile;
-  const int own_begin = min(shared_tiles_of(p, s), ntiles);
-  const int shared_splits = splits_for_tiles(p, own_begin);
+  const int own_begin = min(shared_tiles, ntiles);
+  const int shared_splits = shared_slots_of(p, own_begin);
   const int nsplit = shared_splits + splits_for_tiles(p, ntiles - own_begin);
   if (L == 0) {
     if (split == 0) {
@@ -447,8 +462,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
     }
     return;
   }
-  if (p.seq_group && split == 0 && threadIdx.x == 0 && ntiles - own_begin > p.own_tiles_cap)
-    report(p.dev_err, PKV_DEV_BAD_GROUP);  // more own tokens than the grid covers
+  if (p.seq_group && split == 0 && threadIdx.x == 0) {
+    const int grp = __ldg(p.seq_group + s);
+    // no such group, a longer shared prefix than the launch reserved, or more
+    // own tokens than the grid covers
+    if (grp < 0 || grp >= p.num_groups || splits_for_tiles(p, own_begin) > p.shared_splits_cap ||
+        ntiles - own_begin > p.own_tiles_cap)
+      report(p.dev_err, PKV_DEV_BAD_GROUP);
+  }
   // FUSED in a grouped launch: the new token must fall in the sequence's own
   // tiles (the only ones its own units stream); in a shared tile it would be
   // a token written into a block its whole group reads
@@ -556,33 +577,25 @@ __device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUt
   const int Hq = p.num_q_heads;
 
   const int first = __ldg(p.group_first + grp);
-  const int members = __ldg(p.group_first + grp + 1) - first;
+  const int last = __ldg(p.group_first + grp + 1);
   const int shared = __ldg(p.group_shared + grp);
+  const int members = last - first;
   const int rows = members * G;
-  if (shared <= 0 || members <= 0) return;
-  if (rows > 16 || shared % kTile != 0) {
+  // a malformed group is reported and skipped: members inside the batch, at
+  // most 16 MMA rows, a shared length on a tile boundary within the tables
+  if (first < 0 || members < 0 || last > p.num_seqs || rows > 16 || shared % kTile != 0 ||
+      shared > p.max_blocks * BS) {
     if (threadIdx.x == 0 && g == 0 && split == 0) report(p.dev_err, PKV_DEV_BAD_GROUP);
     return;
   }
+  if (shared <= 0 || members == 0) return;
   const int shared_tiles = shared / kTile;
   const int tile_begin = split * p.partition_tiles;
   if (tile_begin >= shared_tiles) return;
   const int n_here = min(p.partition_tiles, shared_tiles - tile_begin);
 
-  // every member must hold the shared tokens through the leader's blocks
+  // the leader's blocks stream for the whole group: issue them first
   const int32_t* lead = p.block_tables + static_cast<int64_t>(first) * p.max_blocks;
-  {
-    const int blk_lo = tile_begin * kTile / BS;
-    const int blk_hi = (tile_begin + n_here) * kTile / BS;  // shared % BS == 0 (host check)
-    const int nblk = blk_hi - blk_lo;
-    for (int i = threadIdx.x; i < members * nblk; i += kThreads) {
-      const int mem = i / nblk, b = blk_lo + i % nblk;
-      const int32_t* row = p.block_tables + static_cast<int64_t>(first + mem) * p.max_blocks;
-      const int Lm = __ldg(p.context_lens + first + mem);
-      if (__ldg(row + b) != __ldg(lead + b) || Lm < shared) report(p.dev_err, PKV_DEV_BAD_GROUP);
-    }
-  }
-
   TileStream<BS> ts;
   ts.init(smem, &tmap_k, &tmap_v, g, lead, tile_begin, n_here, shared, p);
 
@@ -604,6 +617,27 @@ __device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUt
 #pragma unroll
       for (int kc = 0; kc < 8; ++kc) qa[kc][half] = qa[kc][2 + half] = 0u;
     }
+  }
+
+  // while the first tiles are in flight: every member must belong to this
+  // group, hold at least the shared tokens and map them to the leader's
+  // blocks (loads only in the loop, so the unrolled iterations overlap)
+  {
+    const int blk_lo = tile_begin * kTile / BS;
+    // blocks holding the unit's tiles (the last one partly for BS > 16)
+    const int nblk = ((tile_begin + n_here) * kTile + BS - 1) / BS - blk_lo;
+    const int total = members * nblk;
+    bool bad = false;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const int mem = i / nblk, b = blk_lo + i % nblk;
+      bad |= __ldg(p.block_tables + static_cast<int64_t>(first + mem) * p.max_blocks + b) !=
+             __ldg(lead + b);
+    }
+    if (threadIdx.x < members)
+      bad |= __ldg(p.context_lens + first + threadIdx.x) < shared ||
+             __ldg(p.seq_group + first + threadIdx.x) != grp;
+    if (bad) report(p.dev_err, PKV_DEV_BAD_GROUP);
   }
 
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) paged_attention_merge_kernel(
   L = L < 0 ? 0 : (L > cap ? cap : L);
   const int ntiles = (L + kTile - 1) / kTile;
   const int own_begin = min(shared_tiles_of(p, s), ntiles);
-  const int shared_splits = splits_for_tiles(p, own_begin);
+  const int shared_splits = shared_slots_of(p, own_begin);
   const int nsplit = shared_splits + splits_for_tiles(p, ntiles - own_begin);
   if (nsplit == 0 || (nsplit == 1 && shared_splits == 0)) return;
   const float* ml = p.part_ml + row * p.max_splits * 2;
@@ -201,6 +201,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.num_groups = groups.num_groups;
   p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition *
                     partition;
+  p.shared_splits_cap = shared_splits;
   p.seq_stride = seq_stride_for(num_seqs);
   p.partition_tiles = partition;
   p.scale_log2 = scale * 1.4426950408889634f;

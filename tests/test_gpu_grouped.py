@@ -105,6 +105,36 @@ def test_bad_group_is_reported(ops):
     assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
 
 
+@pytest.mark.parametrize("case", ["group_id_out_of_range", "group_past_batch",
+                                  "member_of_other_group", "shared_longer_than_reserved"])
+def test_malformed_groups_are_reported(ops, case):
+    """Group metadata the kernels cannot trust is reported (BAD_GROUP) and
+    every access stays inside the buffers: a sequence naming no group, a
+    group running past the batch, a member whose group id names another
+    group, a shared prefix longer than the launch reserved workspace for."""
+    prefix = 1024 if case == "shared_longer_than_reserved" else 512
+    q, kc, vc, tables, lens = forked_case(5, [4], 8, 8, 16, prefix)
+    gf = np.array([0, 4], np.int32)
+    sg = np.zeros(4, np.int32)
+    gs = np.array([prefix], np.int32)
+    mx = prefix
+    if case == "group_id_out_of_range":
+        sg[2] = 7
+    elif case == "group_past_batch":
+        gf[1] = 9
+    elif case == "member_of_other_group":
+        gf, gs = np.array([0, 4, 4], np.int32), np.array([prefix, 0], np.int32)
+        sg[2] = 1
+    else:
+        mx = 512                      # the launch reserves one 512-token shared split
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    err = ops.new_error_word()
+    ops.paged_attention_decode_grouped(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
+                                       dev(gf), dev(sg), dev(gs), mx, 700, 0.1, dev_err=err)
+    assert ops.read_error_word(err) == 6      # PKV_DEV_BAD_GROUP
+
+
 def test_own_tokens_beyond_the_stated_bound_are_reported(ops):
     q, kc, vc, tables, lens = forked_case(4, [3, 2], 8, 8, 16, 512, own_max=900)
     gf, sg, gs, mx, mo = ops.shared_prefix_groups(tables, lens, 16, 16)
