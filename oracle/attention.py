@@ -23,23 +23,27 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        path = build_oracle()
-        lib = ctypes.CDLL(path)
-        P = ctypes.c_void_p
-        lib.oracle_paged_attention_decode.argtypes = [
-            P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_double]
-        lib.oracle_paged_attention_decode.restype = ctypes.c_int
-        lib.oracle_paged_attention_decode_rows.argtypes = [
-            P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int]
-        lib.oracle_paged_attention_decode_rows.restype = ctypes.c_int
-        lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
-        lib.oracle_half_to_double.restype = ctypes.c_double
-        lib.oracle_num_threads.argtypes = []
-        lib.oracle_num_threads.restype = ctypes.c_int
-        _lib = lib
+        _lib = bind(ctypes.CDLL(build_oracle()))
     return _lib
+
+
+def bind(lib):
+    """Declare the C oracle's entry points on a loaded library (``_load``; the
+    mutation tests bind deliberately broken copies the same way)."""
+    P = ctypes.c_void_p
+    lib.oracle_paged_attention_decode.argtypes = [
+        P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_double]
+    lib.oracle_paged_attention_decode.restype = ctypes.c_int
+    lib.oracle_paged_attention_decode_rows.argtypes = [
+        P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int]
+    lib.oracle_paged_attention_decode_rows.restype = ctypes.c_int
+    lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_half_to_double.restype = ctypes.c_double
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
+    return lib
 
 
 class OracleError(RuntimeError):
