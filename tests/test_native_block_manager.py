@@ -28,6 +28,7 @@ class Ids:
     "blockmanager_example2.json",
     "blockmanager_example3.json",
     "blockmanager_eviction_trace.json",
+    "blockmanager_duplicate_hash.json",
 ])
 def test_golden_replay_native(bm_mod, name):
     fx = load_golden(name)

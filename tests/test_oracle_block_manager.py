@@ -19,6 +19,7 @@ def make(fx):
     "blockmanager_example2.json",
     "blockmanager_example3.json",
     "blockmanager_eviction_trace.json",
+    "blockmanager_duplicate_hash.json",
 ])
 def test_golden_replay(name):
     fx = load_golden(name)

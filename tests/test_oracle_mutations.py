@@ -82,3 +82,73 @@ def test_unmutated_copy_passes_every_pin(tmp_path, monkeypatch):
 def test_every_mutant_fails_a_pin(tmp_path, monkeypatch, name):
     failed = failing_pins(monkeypatch, build_copy(tmp_path, MUTANTS[name]))
     assert failed, "the mutant '%s' passed every pin" % name
+
+
+# ---- the BlockManager oracle ----------------------------------------------------
+import importlib.util  # noqa: E402
+
+import test_oracle_block_manager as bm_pins  # noqa: E402
+
+BM_SRC = os.path.join(ROOT, "oracle", "block_manager.py")
+
+BM_MUTANTS = {
+    "LIFO free list": ("b = self.free_blocks.popleft()", "b = self.free_blocks.pop()"),
+    "forward-order free": ("for b in reversed(table):", "for b in table:"),
+    "unconditional hash delete": (
+        "            if self.hash_to_block.get(h) == b:\n                del self.hash_to_block[h]",
+        "            self.hash_to_block.pop(h, None)"),
+    "len // bs match limit": ("for h in chain[:(len(tokens) - 1) // bs]:",
+                              "for h in chain[:len(tokens) // bs]:"),
+    "evict the newest": ("b, _ = self.evictable.popitem(last=False)",
+                         "b, _ = self.evictable.popitem(last=True)"),
+    "no copy-on-write": ("        elif self.ref[table[-1]] > 1:", "        elif False:"),
+    "a hit stays evictable": ("                del self.evictable[b]", "                pass"),
+}
+
+BM_PINS = [
+    ("example 1", bm_pins.test_golden_replay, ("blockmanager_example1.json",)),
+    ("example 2", bm_pins.test_golden_replay, ("blockmanager_example2.json",)),
+    ("example 3", bm_pins.test_golden_replay, ("blockmanager_example3.json",)),
+    ("eviction trace", bm_pins.test_golden_replay, ("blockmanager_eviction_trace.json",)),
+    ("duplicate hash", bm_pins.test_golden_replay, ("blockmanager_duplicate_hash.json",)),
+    ("key questions", bm_pins.test_key_questions, ()),
+    ("allocate_requests tables", bm_pins.test_allocate_requests_tables, ()),
+    ("self-check", bm_pins.test_self_check_shared_block_free_twice, ()),
+    ("fork and copy-on-write", bm_pins.test_fork_and_copy_on_write, ()),
+]
+
+
+def load_bm_copy(tmp_path, mutation=None):
+    src = open(BM_SRC).read()
+    if mutation is not None:
+        old, new = mutation
+        assert src.count(old) == 1, "mutation site not unique: %r" % old
+        src = src.replace(old, new)
+    path = tmp_path / "bm_copy.py"
+    path.write_text(src)
+    spec = importlib.util.spec_from_file_location("bm_copy_%d" % id(tmp_path), path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def failing_bm_pins(monkeypatch, mod):
+    monkeypatch.setattr(bm_pins, "BlockManager", mod.BlockManager)
+    monkeypatch.setattr(bm_pins, "OutOfBlocks", mod.OutOfBlocks)
+    failed = []
+    for name, fn, args in BM_PINS:
+        try:
+            fn(*args)
+        except Exception:        # a wrong state, a wrong table or an unexpected raise
+            failed.append(name)
+    return failed
+
+
+def test_unmutated_block_manager_copy_passes_every_pin(tmp_path, monkeypatch):
+    assert failing_bm_pins(monkeypatch, load_bm_copy(tmp_path)) == []
+
+
+@pytest.mark.parametrize("name", sorted(BM_MUTANTS))
+def test_every_block_manager_mutant_fails_a_pin(tmp_path, monkeypatch, name):
+    failed = failing_bm_pins(monkeypatch, load_bm_copy(tmp_path, BM_MUTANTS[name]))
+    assert failed, "the mutant '%s' passed every pin" % name
