@@ -99,6 +99,16 @@ class BlockManager:
     def num_free_blocks(self):
         return int(lib().pkv_bm_num_free_blocks(self._h))
 
+    @property
+    def utilization(self):
+        """Share of the pool in use: 1 - free / num_blocks ("qaqbuyan: vLLM
+        PagedAttention", the block allocator's utilisation), free counting
+        the evictable cached blocks an allocation may reclaim; 0 for an empty
+        pool."""
+        if self.num_blocks == 0:
+            return 0.0
+        return 1.0 - self.num_free_blocks / self.num_blocks
+
     def can_allocate(self, num_tokens):
         return bool(lib().pkv_bm_can_allocate(self._h, int(num_tokens)))
 

@@ -127,3 +127,21 @@ def test_bad_arguments_native(bm_mod):
         bm.slot(1, 2)                  # position past the table
     bm.free(99)                        # unknown id: ignored
     bm.check_invariants()
+
+
+def test_utilization_follows_the_allocator_formula(bm_mod):
+    """1 - free / num_blocks ("qaqbuyan: vLLM PagedAttention", the block
+    allocator), with evictable cached blocks counted as free: an empty pool
+    is 0, allocating k of n blocks gives k / n, freeing returns it to 0
+    whether the freed blocks are cached (evictable) or not."""
+    for cache in (True, False):
+        bm = bm_mod.BlockManager(10, 4, enable_prefix_cache=cache)
+        assert bm.utilization == 0.0
+        bm.allocate(1, list(range(9)))           # 3 blocks
+        assert bm.utilization == pytest.approx(0.3)
+        bm.allocate(2, list(range(100, 117)))    # 5 blocks
+        assert bm.utilization == pytest.approx(0.8)
+        bm.free(1)
+        assert bm.utilization == pytest.approx(0.5)
+        bm.free(2)
+        assert bm.utilization == 0.0
