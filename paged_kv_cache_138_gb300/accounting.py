@@ -12,6 +12,15 @@ def kv_cache_bytes(layers: int, heads: int, head_dim: int, tokens: int,
     return 2 * layers * heads * head_dim * tokens * bytes_per_elem
 
 
+def prefix_sharing_bytes(num_requests: int, prefix_tokens: int, layers: int, heads: int,
+                         head_dim: int, bytes_per_elem: int = 2):
+    """KV bytes of a prompt prefix held by num_requests requests: stored once
+    per request, and stored once for all of them through shared blocks
+    ("qaqbuyan: vLLM PagedAttention", the prefix-sharing example)."""
+    one = kv_cache_bytes(layers, heads, head_dim, prefix_tokens, bytes_per_elem)
+    return num_requests * one, one
+
+
 def step_kv_bytes(context_lens, num_kv_heads: int, head_dim: int, layers: int = 1,
                   bytes_per_elem: int = 2) -> int:
     """Algorithmic K+V bytes one decode step reads (valid tokens only)."""

@@ -65,3 +65,26 @@ def test_kv_sizing_closed_forms():
             assert got / 2 ** 30 == c["gib"]
     # per-step accounting of a decode batch: valid tokens only
     assert accounting.step_kv_bytes([7, 16, 31, 48, 63], 8, 128) == 165 * 8 * 128 * 2 * 2
+
+
+def test_prefix_sharing_savings_example():
+    """The page's prefix-sharing arithmetic, in GiB as printed (rounded the
+    page's way: 3.13, 1.53, 15.3), and the saving as the difference of the
+    printed figures."""
+    fx = load_golden("prefix_sharing_savings.json")
+    from paged_kv_cache_138_gb300 import accounting
+    gib = 2.0 ** 30
+    page = fx["page"]
+    full = accounting.kv_cache_bytes(fx["layers"], fx["heads"], fx["head_dim"], 4096,
+                                     fx["bytes_per_elem"])
+    assert abs(full / gib - page["cache_4096"]) < 0.006
+    separate, shared = accounting.prefix_sharing_bytes(fx["num_requests"], fx["prefix_tokens"],
+                                                       fx["layers"], fx["heads"],
+                                                       fx["head_dim"], fx["bytes_per_elem"])
+    assert abs(shared / gib - page["per_request"]) < 0.005
+    assert shared == accounting.kv_cache_bytes(fx["layers"], fx["heads"], fx["head_dim"],
+                                               fx["prefix_tokens"], fx["bytes_per_elem"])
+    assert abs(shared / gib - page["shared"]) < 0.005
+    assert abs(separate / gib - page["separate"]) < 0.05
+    assert abs(round(separate / gib, 1) - round(shared / gib, 2) - page["saving"]) < 1e-9
+    assert round(100 * (1 - shared / separate)) == page["saving_pct"]
