@@ -492,6 +492,8 @@ typedef struct pkv_decode_launch {
   size_t workspace_bytes;
   float scale;
   int32_t* dev_err;
+  int32_t meta_staged;         /* nonzero: pkv_sched_stage_decode already copied this
+                                  step's metadata into meta (skip the copy) */
 } pkv_decode_launch;
 
 /* Device staging bytes pkv_sched_launch_decode needs. */
@@ -510,6 +512,15 @@ size_t pkv_sched_meta_bytes(const pkv_scheduler* sched);
  * max_batch int32), the metadata goes to the device in one copy. */
 int pkv_sched_launch_decode(const pkv_scheduler* sched, const pkv_sched_step_out* out,
                             const pkv_decode_launch* d, void* stream);
+
+/* The metadata copy of pkv_sched_launch_decode alone, enqueued on `stream`
+ * (e.g. a copy stream, so that it overlaps the previous step's kernels): the
+ * caller then orders the decode stream after it (an event) and launches with
+ * d->meta_staged set.  d->meta must not be in use by an earlier step's kernels
+ * still running (double-buffer it), and out's pinned arrays must stay
+ * untouched until the copy has completed. */
+int pkv_sched_stage_decode(const pkv_scheduler* sched, const pkv_sched_step_out* out,
+                           const pkv_decode_launch* d, void* stream);
 
 /* Requests waiting or running. */
 int64_t pkv_sched_num_unfinished(const pkv_scheduler* sched);

@@ -56,6 +56,7 @@ SIGNATURES = {
     "pkv_sched_num_unfinished": (_I64, [_P]),
     "pkv_sched_meta_bytes": (_SZ, [_P]),
     "pkv_sched_launch_decode": (_I, [_P, _P, _P, _P]),
+    "pkv_sched_stage_decode": (_I, [_P, _P, _P, _P]),
     "pkv_sched_request_tokens": (_I64, [_P, _I64, _P, _I64]),
     "pkv_bm_create": (_P, [_I64, _I, _I, _P]),
     "pkv_bm_destroy": (None, [_P]),

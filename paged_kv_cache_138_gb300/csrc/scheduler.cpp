@@ -327,6 +327,79 @@ size_t pkv_sched_meta_bytes(const pkv_scheduler* s) {
   return B * 8 + (B * s->max_blocks + B + 3 * B + 1) * 4 + 64;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Where the step's metadata lives in the device staging area: slots (int64,
+// unused by the fused launches), then int32 tables | lengths | group_first |
+// seq_group | group_shared.
+struct Staging {
+  int32_t *tables, *lens, *gfirst, *gseq, *gshared;
+};
+
+Staging staging_of(const pkv_scheduler* s, void* meta_ptr) {
+  uint8_t* meta = static_cast<uint8_t*>(meta_ptr);
+  const size_t MB = static_cast<size_t>(s->max_batch);
+  Staging g;
+  g.tables = reinterpret_cast<int32_t*>(meta + MB * 8);
+  g.lens = g.tables + MB * s->max_blocks;
+  g.gfirst = g.lens + MB;
+  g.gseq = g.gfirst + MB + 1;
+  g.gshared = g.gseq + MB;
+  return g;
+}
+
+bool grouped_step(const pkv_sched_step_out* o) {
+  return o->num_groups > 0 && o->max_shared_tokens > 0;
+}
+
+// Host -> device copy of a planned step's tables, lengths and groups: one copy
+// when out's arrays lie back to back in the staging layout, else one per array.
+int copy_metadata(const pkv_scheduler* s, const pkv_sched_step_out* o, const Staging& g,
+                  cudaStream_t st) {
+  const int B = o->num_batch;
+  const int mb = s->max_blocks;
+  const size_t MB = static_cast<size_t>(s->max_batch);
+  const bool grouped = grouped_step(o);
+  const bool packed = o->context_lens == o->block_tables + MB * mb &&
+                      o->group_first == o->context_lens + MB &&
+                      o->seq_group == o->group_first + MB + 1 && o->group_shared == o->seq_group + MB;
+  if (packed) {
+    const size_t n = grouped ? MB * mb + MB + 3 * MB + 1 : MB * mb + MB;
+    return cudaMemcpyAsync(g.tables, o->block_tables, sizeof(int32_t) * n,
+                           cudaMemcpyHostToDevice, st) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(g.tables, o->block_tables, sizeof(int32_t) * B * mb, cudaMemcpyHostToDevice,
+                      st) != cudaSuccess ||
+      cudaMemcpyAsync(g.lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
+          cudaSuccess)
+    return PKV_ERR_CUDA;
+  if (grouped &&
+      (cudaMemcpyAsync(g.gfirst, o->group_first, sizeof(int32_t) * (o->num_groups + 1),
+                       cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaMemcpyAsync(g.gseq, o->seq_group, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
+           cudaSuccess ||
+       cudaMemcpyAsync(g.gshared, o->group_shared, sizeof(int32_t) * o->num_groups,
+                       cudaMemcpyHostToDevice, st) != cudaSuccess))
+    return PKV_ERR_CUDA;
+  return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_sched_stage_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
+                           const pkv_decode_launch* d, void* stream) {
+  if (!s || !o || !d || !d->meta || d->meta_bytes < pkv_sched_meta_bytes(s))
+    return PKV_ERR_INVALID_ARG;
+  if (o->num_batch == 0) return PKV_OK;
+  return copy_metadata(s, o, staging_of(s, d->meta), static_cast<cudaStream_t>(stream));
+}
+
 int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
                             const pkv_decode_launch* d, void* stream) {
   if (!s || !o || !d || !d->meta || d->meta_bytes < pkv_sched_meta_bytes(s))
@@ -335,51 +408,21 @@ int pkv_sched_launch_decode(const pkv_scheduler* s, const pkv_sched_step_out* o,
   if (B == 0) return PKV_OK;
   const int mb = s->max_blocks;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* meta = static_cast<uint8_t*>(d->meta);
-  int64_t* slots = reinterpret_cast<int64_t*>(meta);
-  int32_t* tables = reinterpret_cast<int32_t*>(meta + static_cast<size_t>(s->max_batch) * 8);
-  int32_t* lens = tables + static_cast<size_t>(s->max_batch) * mb;
-  int32_t* groups = lens + s->max_batch;  // group_first | seq_group | group_shared
-  const bool grouped = o->num_groups > 0 && o->max_shared_tokens > 0;
+  const Staging g = staging_of(s, d->meta);
   // the fused launches recompute each new token's slot from its table row, so
   // the step's slots stay on the host
-  (void)slots;
-  int32_t* gfirst = groups;
-  int32_t* gseq = groups + s->max_batch + 1;
-  int32_t* gshared = gseq + s->max_batch;
-  // host arrays laid out like the staging area (tables | lens | groups): one copy
-  const size_t MB = static_cast<size_t>(s->max_batch);
-  const bool packed = o->context_lens == o->block_tables + MB * mb &&
-                      o->group_first == o->context_lens + MB &&
-                      o->seq_group == o->group_first + MB + 1 && o->group_shared == o->seq_group + MB;
-  if (packed) {
-    const size_t n = grouped ? MB * mb + MB + 3 * MB + 1 : MB * mb + MB;
-    if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * n, cudaMemcpyHostToDevice, st) !=
-        cudaSuccess)
-      return PKV_ERR_CUDA;
-  } else if (cudaMemcpyAsync(tables, o->block_tables, sizeof(int32_t) * B * mb,
-                             cudaMemcpyHostToDevice, st) != cudaSuccess ||
-             cudaMemcpyAsync(lens, o->context_lens, sizeof(int32_t) * B, cudaMemcpyHostToDevice,
-                             st) != cudaSuccess) {
-    return PKV_ERR_CUDA;
+  if (!d->meta_staged) {
+    const int rc = copy_metadata(s, o, g, st);
+    if (rc != PKV_OK) return rc;
   }
-  if (grouped && !packed) {
-    if (cudaMemcpyAsync(gfirst, o->group_first, sizeof(int32_t) * (o->num_groups + 1),
-                        cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(gseq, o->seq_group, sizeof(int32_t) * B, cudaMemcpyHostToDevice, st) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(gshared, o->group_shared, sizeof(int32_t) * o->num_groups,
-                        cudaMemcpyHostToDevice, st) != cudaSuccess)
-      return PKV_ERR_CUDA;
-  }
-  if (grouped)
+  if (grouped_step(o))
     return pkv_paged_attention_decode_grouped_fused(
-        d->out, d->q, d->k_new, d->v_new, d->k_cache, d->v_cache, tables, lens, gfirst, gseq,
-        gshared, o->num_groups, o->max_shared_tokens, o->max_own_tokens, B, d->num_q_heads,
-        d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks, mb, d->scale, d->workspace,
-        d->workspace_bytes, d->dev_err, stream);
+        d->out, d->q, d->k_new, d->v_new, d->k_cache, d->v_cache, g.tables, g.lens, g.gfirst,
+        g.gseq, g.gshared, o->num_groups, o->max_shared_tokens, o->max_own_tokens, B,
+        d->num_q_heads, d->num_kv_heads, d->head_dim, s->block_size, d->num_blocks, mb, d->scale,
+        d->workspace, d->workspace_bytes, d->dev_err, stream);
   return pkv_paged_attention_decode_fused(d->out, d->q, d->k_new, d->v_new, d->k_cache,
-                                          d->v_cache, tables, lens, B, d->num_q_heads,
+                                          d->v_cache, g.tables, g.lens, B, d->num_q_heads,
                                           d->num_kv_heads, d->head_dim, s->block_size,
                                           d->num_blocks, mb, d->scale, d->workspace,
                                           d->workspace_bytes, d->dev_err, stream);

@@ -53,7 +53,7 @@ class _DecodeLaunch(ctypes.Structure):
         ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p),
         ("out", ctypes.c_void_p), ("meta", ctypes.c_void_p), ("meta_bytes", ctypes.c_size_t),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-        ("scale", ctypes.c_float), ("dev_err", ctypes.c_void_p),
+        ("scale", ctypes.c_float), ("dev_err", ctypes.c_void_p), ("meta_staged", ctypes.c_int32),
     ]
 
 
@@ -147,23 +147,31 @@ class NativeServingDriver:
         self.dev_err = ops.new_error_word(self.dev)
         self.scale = 1.0 / float(np.sqrt(head_dim))
         self.steps = 0
-        # the decode launch: one native call per step (metadata copies, cache
-        # write, plain or grouped attention)
-        self.meta = torch.empty(int(lib().pkv_sched_meta_bytes(self._h)), dtype=torch.uint8,
-                                device=self.dev)
-        dl = _DecodeLaunch()
-        dl.k_cache, dl.v_cache = self.k_cache.data_ptr(), self.v_cache.data_ptr()
-        dl.num_blocks = num_blocks
-        dl.num_q_heads, dl.num_kv_heads, dl.head_dim = num_q_heads, num_kv_heads, head_dim
-        dl.q, dl.k_new, dl.v_new = self.q.data_ptr(), self.k_new.data_ptr(), self.v_new.data_ptr()
-        dl.out = self.out.data_ptr()
-        dl.meta, dl.meta_bytes = self.meta.data_ptr(), self.meta.numel()
+        # the decode launch: one native call per step (cache write, plain or
+        # grouped attention).  Each set of step arrays has its own device
+        # staging for the step's metadata, copied on a side stream while the
+        # previous step's kernels run (pkv_sched_stage_decode); the decode
+        # stream waits for that copy only.
+        meta_bytes = int(lib().pkv_sched_meta_bytes(self._h))
         ws = self.workspace
-        dl.workspace = ws.data_ptr() if ws is not None else None
-        dl.workspace_bytes = ws.numel() if ws is not None else 0
-        dl.scale = self.scale
-        dl.dev_err = self.dev_err.data_ptr()
-        self.launch = dl
+        self.copy_stream = torch.cuda.Stream(self.dev) if pin else None
+        for st in self.sets:
+            st["meta"] = torch.empty(meta_bytes, dtype=torch.uint8, device=self.dev)
+            dl = _DecodeLaunch()
+            dl.k_cache, dl.v_cache = self.k_cache.data_ptr(), self.v_cache.data_ptr()
+            dl.num_blocks = num_blocks
+            dl.num_q_heads, dl.num_kv_heads, dl.head_dim = num_q_heads, num_kv_heads, head_dim
+            dl.q, dl.k_new, dl.v_new = (self.q.data_ptr(), self.k_new.data_ptr(),
+                                        self.v_new.data_ptr())
+            dl.out = self.out.data_ptr()
+            dl.meta, dl.meta_bytes = st["meta"].data_ptr(), meta_bytes
+            dl.workspace = ws.data_ptr() if ws is not None else None
+            dl.workspace_bytes = ws.numel() if ws is not None else 0
+            dl.scale = self.scale
+            dl.dev_err = self.dev_err.data_ptr()
+            dl.meta_staged = 1 if pin else 0
+            st["launch"] = dl
+            st["staged"] = torch.cuda.Event() if pin else None
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -213,6 +221,15 @@ class NativeServingDriver:
         cuda = self.dev.type == "cuda"
         # one stream for the whole step, looked up once
         stream = torch.cuda.current_stream(self.dev) if cuda else None
+        if o.num_batch and st["staged"] is not None:
+            # this set's staging was last read by the step two back, which the
+            # event above has seen finish; the copy runs beside this step's
+            # first launches and the previous step's kernels
+            rc = lib().pkv_sched_stage_decode(self._h, ctypes.byref(o), ctypes.byref(st["launch"]),
+                                              ctypes.c_void_p(self.copy_stream.cuda_stream))
+            if rc != PKV_OK:
+                raise PagedKVError(rc, "sched_stage_decode")
+            st["staged"].record(self.copy_stream)
         caches = ([self.k_cache, self.v_cache], [self.host_k, self.host_v])
         if o.num_swap_in:
             ops.swap_blocks(caches[1], caches[0], self._h2d(t["swap_in_pairs"][:o.num_swap_in]),
@@ -238,8 +255,10 @@ class NativeServingDriver:
                "groups": 0, "shared_tokens": 0}
         if B:
             self.values.decode_into(self, res["rids"], res["positions"], B, stream=stream)
+            if st["staged"] is not None:
+                stream.wait_event(st["staged"])
             rc = lib().pkv_sched_launch_decode(
-                self._h, ctypes.byref(o), ctypes.byref(self.launch),
+                self._h, ctypes.byref(o), ctypes.byref(st["launch"]),
                 ctypes.c_void_p(stream.cuda_stream) if cuda else None)
             if rc != PKV_OK:
                 raise PagedKVError(rc, "sched_launch_decode")
