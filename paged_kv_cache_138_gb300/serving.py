@@ -172,6 +172,9 @@ class NativeServingDriver:
             dl.meta_staged = 1 if pin else 0
             st["launch"] = dl
             st["staged"] = torch.cuda.Event() if pin else None
+            # device copy of the set's prefill slots (staged with the metadata)
+            st["prefill_slots_dev"] = torch.empty(B * mb * block_size, dtype=torch.int64,
+                                                  device=self.dev)
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -221,15 +224,23 @@ class NativeServingDriver:
         cuda = self.dev.type == "cuda"
         # one stream for the whole step, looked up once
         stream = torch.cuda.current_stream(self.dev) if cuda else None
-        if o.num_batch and st["staged"] is not None:
+        staged = st["staged"] is not None and (o.num_batch or o.num_prefill)
+        if staged:
             # this set's staging was last read by the step two back, which the
-            # event above has seen finish; the copy runs beside this step's
+            # event above has seen finish; the copies run beside this step's
             # first launches and the previous step's kernels
-            rc = lib().pkv_sched_stage_decode(self._h, ctypes.byref(o), ctypes.byref(st["launch"]),
-                                              ctypes.c_void_p(self.copy_stream.cuda_stream))
-            if rc != PKV_OK:
-                raise PagedKVError(rc, "sched_stage_decode")
-            st["staged"].record(self.copy_stream)
+            cs = self.copy_stream
+            if o.num_prefill:
+                with torch.cuda.stream(cs):
+                    st["prefill_slots_dev"][:o.num_prefill].copy_(
+                        t["prefill_slots"][:o.num_prefill], non_blocking=True)
+            if o.num_batch:
+                rc = lib().pkv_sched_stage_decode(self._h, ctypes.byref(o),
+                                                  ctypes.byref(st["launch"]),
+                                                  ctypes.c_void_p(cs.cuda_stream))
+                if rc != PKV_OK:
+                    raise PagedKVError(rc, "sched_stage_decode")
+            st["staged"].record(cs)
         caches = ([self.k_cache, self.v_cache], [self.host_k, self.host_v])
         if o.num_swap_in:
             ops.swap_blocks(caches[1], caches[0], self._h2d(t["swap_in_pairs"][:o.num_swap_in]),
@@ -238,8 +249,13 @@ class NativeServingDriver:
             n = o.num_prefill
             k, v = self.values.prefill(self, a["prefill_rids"][:n], a["prefill_positions"][:n],
                                        stream=stream)
-            ops.reshape_and_cache(k, v, self._h2d(t["prefill_slots"][:n]), self.k_cache,
-                                  self.v_cache, dev_err=self.dev_err, stream=stream)
+            if staged:
+                stream.wait_event(st["staged"])
+                slots = st["prefill_slots_dev"][:n]
+            else:
+                slots = self._h2d(t["prefill_slots"][:n])
+            ops.reshape_and_cache(k, v, slots, self.k_cache, self.v_cache, dev_err=self.dev_err,
+                                  stream=stream)
         if o.num_swap_out:
             ops.swap_blocks(caches[0], caches[1], self._h2d(t["swap_out_pairs"][:o.num_swap_out]),
                             dev_err=self.dev_err, stream=stream)
@@ -255,7 +271,7 @@ class NativeServingDriver:
                "groups": 0, "shared_tokens": 0}
         if B:
             self.values.decode_into(self, res["rids"], res["positions"], B, stream=stream)
-            if st["staged"] is not None:
+            if staged:
                 stream.wait_event(st["staged"])
             rc = lib().pkv_sched_launch_decode(
                 self._h, ctypes.byref(o), ctypes.byref(st["launch"]),
