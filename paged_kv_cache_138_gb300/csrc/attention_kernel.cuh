@@ -693,6 +693,11 @@ template <int G, int BS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                  const __grid_constant__ CUtensorMap tmap_v, const Params p) {
+  // launched as a programmatic dependent of the stream's previous kernel: the
+  // CTAs may be placed while it finishes; nothing is read before this wait,
+  // which returns once that kernel has completed and its writes are visible
+  // (a no-op after any other operation)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int s = static_cast<int>(static_cast<int64_t>(blockIdx.y) * p.seq_stride % p.num_seqs);
   split_body<G, BS, FUSED>(tmap_k, tmap_v, p, aligned_smem(), blockIdx.x, s, blockIdx.z);
 }
@@ -712,6 +717,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_attention_grouped_kernel(const __grid_constant__ CUtensorMap tmap_k,
                                    const __grid_constant__ CUtensorMap tmap_v, const Params p,
                                    int shared_splits, int own_splits, int shared_stride) {
+  // launched as a programmatic dependent of the stream's previous kernel: the
+  // CTAs may be placed while it finishes; nothing is read before this wait,
+  // which returns once that kernel has completed and its writes are visible
+  // (a no-op after any other operation)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   uint8_t* smem = aligned_smem();
   int u = blockIdx.x;
   const int n_shared = p.num_kv_heads * p.num_groups * shared_splits;
@@ -754,9 +764,21 @@ int launch_one(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p, in
   static std::atomic<uint8_t> opted_in[64];
   const int rc = opt_in_smem(paged_attention_split_kernel<G, BS, FUSED>, opted_in);
   if (rc != PKV_OK) return rc;
-  dim3 grid(p.num_kv_heads, p.num_seqs, private_splits);
-  paged_attention_split_kernel<G, BS, FUSED><<<grid, kThreads, Smem::alloc, stream>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  // programmatic dependent launch: see the wait at the kernel's entry
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.num_kv_heads, p.num_seqs, private_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem::alloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_attention_split_kernel<G, BS, FUSED>, mk, mv, p) ==
+                 cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 template <int G, int BS, bool FUSED>
@@ -770,10 +792,21 @@ int launch_grouped(const CUtensorMap& mk, const CUtensorMap& mv, const Params& p
                          static_cast<int64_t>(p.num_seqs) * own_splits);
   if (units <= 0) return PKV_OK;
   if (units > INT32_MAX) return PKV_ERR_UNSUPPORTED;
-  paged_attention_grouped_kernel<G, BS, FUSED>
-      <<<static_cast<unsigned>(units), kThreads, Smem::alloc, stream>>>(
-          mk, mv, p, shared_splits, own_splits, shared_stride);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  // programmatic dependent launch: see the wait at the kernel's entry
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem::alloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_attention_grouped_kernel<G, BS, FUSED>, mk, mv, p,
+                            shared_splits, own_splits, shared_stride) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
 }
 
 // Host launchers for one block size (defined in attention_bs*.cu).

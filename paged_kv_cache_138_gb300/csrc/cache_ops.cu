@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(kThreads)
                              const int64_t* __restrict__ slots, uint4* __restrict__ kc,
                              uint4* __restrict__ vc, int64_t total, int row_vecs,
                              int64_t num_slots, int32_t* dev_err) {
+  // a programmatically dependent launch that follows (the attention kernel)
+  // may place its CTAs while this grid runs; it reads nothing before this
+  // grid has completed
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   if (idx >= total) return;
   const int64_t i = idx / row_vecs;
@@ -69,6 +73,10 @@ struct LayerPtrs {
 __global__ void __launch_bounds__(kThreads)
     copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs, const int64_t* __restrict__ pairs,
                        int64_t block_vecs, int64_t num_blocks, int32_t* dev_err) {
+  // a programmatically dependent launch that follows (the attention kernel)
+  // may place its CTAs while this grid runs; it reads nothing before this
+  // grid has completed
+  asm volatile("griddepcontrol.launch_dependents;");
   const int pair = blockIdx.x, layer = blockIdx.y;
   const int64_t src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {

@@ -21,6 +21,10 @@ namespace attn {
 constexpr int kMergeRows = 8;
 
 __global__ void __launch_bounds__(kMergeRows * 32) paged_attention_merge_kernel(const Params p) {
+  // a programmatically dependent launch that follows (the attention kernel)
+  // may place its CTAs while this grid runs; it reads nothing before this
+  // grid has completed
+  asm volatile("griddepcontrol.launch_dependents;");
   // launched as a programmatic dependent of the attention kernel: CTAs may be
   // resident before it finishes; wait here until its writes are visible (a
   // no-op for an ordinary launch)

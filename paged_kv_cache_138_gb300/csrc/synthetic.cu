@@ -53,6 +53,10 @@ __device__ __forceinline__ float normal_at(uint64_t seed, uint64_t j) {
 
 __global__ void __launch_bounds__(kThreads)
     fill_normal_f16_kernel(__half* __restrict__ dst, int64_t n, uint64_t seed, uint64_t offset) {
+  // a programmatically dependent launch that follows (the attention kernel)
+  // may place its CTAs while this grid runs; it reads nothing before this
+  // grid has completed
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads * kPerThread;
   for (int64_t base = (static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) * kPerThread;
        base < n; base += stride) {

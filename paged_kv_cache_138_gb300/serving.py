@@ -270,9 +270,9 @@ class NativeServingDriver:
                "swap_out": o.num_swap_out, "kv_tokens": int(a["context_lens"][:B].sum()),
                "groups": 0, "shared_tokens": 0}
         if B:
-            self.values.decode_into(self, res["rids"], res["positions"], B, stream=stream)
-            if staged:
+            if staged:   # before the fill, so the fill and the decode launch stay adjacent
                 stream.wait_event(st["staged"])
+            self.values.decode_into(self, res["rids"], res["positions"], B, stream=stream)
             rc = lib().pkv_sched_launch_decode(
                 self._h, ctypes.byref(o), ctypes.byref(st["launch"]),
                 ctypes.c_void_p(stream.cuda_stream) if cuda else None)
