@@ -158,9 +158,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_oracle_sample(step, layer, seqs, heads, min_seconds=0.0):
-    """Time the fp64 oracle on a sample of sequences of one layer (host cores),
-    repeating the sample until at least ``min_seconds`` of oracle time.
+def cpu_oracle_sample(step, layer, seqs, heads, min_seconds=0.0, threads=None):
+    """Time the fp64 oracle on a sample of sequences of one layer (host cores,
+    or ``threads`` of them), repeating the sample until at least
+    ``min_seconds`` of oracle time.
     Returns (seconds, KV bytes attended over in that time, threads)."""
     import numpy as np
 
@@ -190,14 +191,20 @@ def cpu_oracle_sample(step, layer, seqs, heads, min_seconds=0.0):
     frac_heads = len(heads) / w.num_q_heads
     kv_once = accounting.step_kv_bytes(lens, w.num_kv_heads, w.head_dim) * frac_heads
     dt, kv = 0.0, 0.0
-    while True:
-        t0 = time.perf_counter()
-        oc.reshape_and_cache(kn, vn, slots, kc, vc)
-        oa.paged_attention_decode_rows(q, kc, vc, t2, lens, w.scale, si, hi)
-        dt += time.perf_counter() - t0
-        kv += kv_once
-        if dt >= min_seconds:
-            return dt, kv, oa.num_threads()
+    all_threads = oa.num_threads()
+    if threads is not None:
+        oa.set_num_threads(threads)
+    try:
+        while True:
+            t0 = time.perf_counter()
+            oc.reshape_and_cache(kn, vn, slots, kc, vc)
+            oa.paged_attention_decode_rows(q, kc, vc, t2, lens, w.scale, si, hi)
+            dt += time.perf_counter() - t0
+            kv += kv_once
+            if dt >= min_seconds:
+                return dt, kv, oa.num_threads()
+    finally:
+        oa.set_num_threads(all_threads)
 
 
 def setup(args, device, rank=0):
@@ -466,6 +473,12 @@ def run_ours(args):
                "sample": "%d random of %d sequences x all %d heads of layer 0 (reshape_and_cache "
                          "+ attention), repeated for %.1f s (fp64 C oracle, OpenMP)" % (
                              len(seqs), S, w.num_q_heads, tot_t)}
+        # the same oracle on one core, on the first two of those sequences
+        t1, kv1, _ = cpu_oracle_sample(step, 0, seqs[:2], list(range(w.num_q_heads)),
+                                       min_seconds=3.0, threads=1)
+        cpu["single_thread"] = {"value": kv1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                                "sample": "%d sequences x all %d heads, repeated for %.1f s" % (
+                                    min(2, len(seqs)), w.num_q_heads, t1)}
     launches = step.kernel_launches_per_step() + (1 if batch.cow_pairs.shape[0] else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,

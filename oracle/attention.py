@@ -43,6 +43,8 @@ def bind(lib):
     lib.oracle_half_to_double.restype = ctypes.c_double
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
+    lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+    lib.oracle_set_num_threads.restype = None
     return lib
 
 
@@ -70,6 +72,11 @@ def half_to_double(bits: int) -> float:
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's later calls use (OpenMP)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, scale):

@@ -170,3 +170,13 @@ int oracle_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads later calls use (n >= 1); for timing the oracle on one core. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
