@@ -90,6 +90,49 @@ def test_llama2_7b_32_layer_full_size(native_lib):
     run_and_check("llama2-7b-32layer", [0, 31], 96)
 
 
+def test_llama2_7b_every_layer_sampled(native_lib):
+    """All 32 layers of the 7B step.  Per layer a few sequences are drawn and
+    only their blocks are copied to the host before the step (compacted,
+    tables renumbered); the oracle applies its own cache write of those
+    sequences' new tokens and evaluates every query head of them."""
+    from paged_kv_cache_138_gb300.engine import DecodeStep
+    from paged_kv_cache_138_gb300.scenario import prepare_batch
+    w = wl.WORKLOADS["llama2-7b-32layer"]
+    batch = prepare_batch(w)
+    tables, lens, slots, pairs, nb = oracle_batch(w)
+    assert len(pairs) == 0
+    step = DecodeStep(batch)
+    rng = np.random.default_rng(79)
+    S, Hq, bs = batch.num_seqs, w.num_q_heads, w.block_size
+    picked = {}
+    for i in range(step.num_layers):
+        seqs = np.sort(rng.choice(S, size=3, replace=False))
+        blocks = sorted({int(b) for s in seqs for b in tables[s][:-(-int(lens[s]) // bs)]})
+        idx = torch.tensor(blocks, dtype=torch.long, device=step.k_cache.device)
+        picked[i] = (seqs, blocks, step.k_cache[i].index_select(0, idx).cpu().numpy(),
+                     step.v_cache[i].index_select(0, idx).cpu().numpy())
+    out = step.run()
+    step.check_errors()
+    torch.cuda.synchronize()
+    worst = 0.0
+    for i, (seqs, blocks, kc, vc) in picked.items():
+        remap = {b: j for j, b in enumerate(blocks)}
+        t2 = np.array([[remap.get(int(b), -1) if b >= 0 else -1 for b in tables[s]]
+                       for s in seqs], dtype=np.int32)
+        s2 = np.array([remap[int(slots[s]) // bs] * bs + int(slots[s]) % bs for s in seqs],
+                      dtype=np.int64)
+        oc.reshape_and_cache(step.k_new[i].cpu().numpy()[seqs], step.v_new[i].cpu().numpy()[seqs],
+                             s2, kc, vc)
+        q = step.q[i].cpu().numpy()[seqs]
+        si = np.repeat(np.arange(len(seqs), dtype=np.int32), Hq)
+        hi = np.tile(np.arange(Hq, dtype=np.int32), len(seqs))
+        ref = oa.paged_attention_decode_rows(q, kc, vc, t2, lens[seqs], w.scale, si, hi)
+        gpu = out[i].cpu().numpy().astype(np.float64)[seqs[si], hi]
+        assert np.isfinite(gpu).all()
+        worst = max(worst, float(np.abs(gpu - ref).max()))
+    assert worst <= TOL, "max abs error %.3g" % worst
+
+
 def test_graph_replay_matches_eager(native_lib):
     """One decode step captured in a CUDA graph gives the eager step's bits."""
     from paged_kv_cache_138_gb300.engine import DecodeStep
