@@ -430,6 +430,21 @@ def run_ours(args):
         graph_ms = sum(per_step_timed(args.steps, step.replay)) / args.steps
     step.check_errors()
 
+    # ---- a step that L2 could partly keep between steps (under 8x its size):
+    # also timed step by step with L2 flushed after each (besides the main
+    # figure, which runs back to back on inputs larger than L2)
+    flushed = None
+    if flush_buf is None and step_bytes < 8 * l2_bytes:
+        flush_buf = torch.empty(max(4 * l2_bytes, 512 << 20), dtype=torch.uint8, device=device)
+        n_fl = min(args.steps, 500)
+        fl_ms = sum(per_step_timed(n_fl, one_step)) / n_fl
+        flushed = {"ms_per_step": fl_ms, "value": world * kv_bytes / (fl_ms / 1e3) / 1e9,
+                   "unit": "GB/s", "steps": n_fl,
+                   "note": "each step between its own events, L2 flushed by a %d MiB write "
+                           "after each" % (flush_buf.numel() >> 20)}
+        flush_buf = None
+        step.check_errors()
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -512,6 +527,7 @@ def run_ours(args):
                 "mean_ms_per_step": e2e_mean_ms, "windows": len(windows),
                 "steps_per_window": chunk,
                 "timing": "median of %d windows of %d pipelined steps" % (len(windows), chunk)},
+        "l2_flushed": flushed,
         "graph": {"ms_per_step": graph_ms, "value": world * kv_bytes / (graph_ms / 1e3) / 1e9,
                   "unit": "GB/s", "note": "same step replayed from a CUDA graph"},
         "gpu_launches": launches * args.steps,
