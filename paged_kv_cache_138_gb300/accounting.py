@@ -21,6 +21,17 @@ def prefix_sharing_bytes(num_requests: int, prefix_tokens: int, layers: int, hea
     return num_requests * one, one
 
 
+def slot_utilization(tokens: int, reserved_tokens: int) -> float:
+    """Share of reserved KV slots that hold tokens: a contiguous reservation of
+    the maximum length ("qaqbuyan: vLLM PagedAttention", the pre-allocation
+    example) against paging, whose reservation is ceil(tokens / bs) * bs."""
+    return tokens / reserved_tokens if reserved_tokens else 0.0
+
+
+def paged_reserved_tokens(tokens: int, block_size: int) -> int:
+    return -(-int(tokens) // block_size) * block_size
+
+
 def step_kv_bytes(context_lens, num_kv_heads: int, head_dim: int, layers: int = 1,
                   bytes_per_elem: int = 2) -> int:
     """Algorithmic K+V bytes one decode step reads (valid tokens only)."""

@@ -88,3 +88,31 @@ def test_prefix_sharing_savings_example():
     assert abs(separate / gib - page["separate"]) < 0.05
     assert abs(round(separate / gib, 1) - round(shared / gib, 2) - page["saving"]) < 1e-9
     assert round(100 * (1 - shared / separate)) == page["saving_pct"]
+
+
+def test_concurrent_requests_and_preallocation_examples():
+    """The page's sizing of 10 concurrent 4096-token requests (in GiB, its
+    weights in decimal GB, the total the sum of the printed figures) and its
+    pre-allocation utilisations; paging's reservation for the same lengths
+    (whole 16-token blocks) for contrast."""
+    fx = load_golden("kv_sizing_examples.json")
+    from paged_kv_cache_138_gb300 import accounting
+    m, c = fx["model"], fx["concurrent"]
+    one = accounting.kv_cache_bytes(m["layers"], m["heads"], m["head_dim"], c["tokens"],
+                                    m["bytes_per_elem"])
+    from decimal import ROUND_HALF_UP, Decimal
+    # the page multiplies its per-request figure, rounded half-up to 3.13
+    # (exactly 3.125 GiB), by the request count
+    per = Decimal(one) / Decimal(2 ** 30)
+    printed = float(per.quantize(Decimal("0.01"), rounding=ROUND_HALF_UP)) * c["requests"]
+    assert abs(printed - c["cache_total"]) < 1e-9
+    assert abs(c["requests"] * float(per) - c["cache_total"]) < 0.06     # exact: 31.25
+    assert round(100 * printed / 80) == c["share_of_80"]
+    weights = m["params"] * m["bytes_per_elem"] / 1e9
+    assert weights == c["weights"]
+    assert abs(printed + weights - c["total"]) < 1e-9
+    pre = fx["preallocation"]
+    for used, pct in pre["cases"]:
+        assert round(100 * accounting.slot_utilization(used, pre["reserved"]), 1) == pct
+        paged = accounting.slot_utilization(used, accounting.paged_reserved_tokens(used, 16))
+        assert paged > 0.78 and accounting.paged_reserved_tokens(used, 16) - used < 16
