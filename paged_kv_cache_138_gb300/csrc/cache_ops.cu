@@ -69,34 +69,43 @@ struct LayerPtrs {
   uint4* v[kMaxLayersPerLaunch];
 };
 
-// grid (pairs, layers, 2 caches): one CTA copies one block of one cache.
+// grid (pairs x chunks, layers, 2 caches): a CTA copies one chunk of one block
+// of one cache, each thread keeping kCopyUnroll 16-byte loads in flight.  A
+// 128 KB block (16 tokens x 32 heads x 256 B) is 4 chunks, so a step's few
+// hundred copy-on-write pairs still give every SM several CTAs: one CTA per
+// block left the copy latency-bound.
+constexpr int kCopyUnroll = 8;
+constexpr int64_t kCopyChunkVecs = static_cast<int64_t>(kThreads) * kCopyUnroll;
+
 __global__ void __launch_bounds__(kThreads)
     copy_blocks_kernel(const __grid_constant__ LayerPtrs ptrs, const int64_t* __restrict__ pairs,
-                       int64_t block_vecs, int64_t num_blocks, int32_t* dev_err) {
+                       int64_t block_vecs, int chunks, int64_t num_blocks, int32_t* dev_err) {
   // a programmatically dependent launch that follows (the attention kernel)
   // may place its CTAs while this grid runs; it reads nothing before this
   // grid has completed
   asm volatile("griddepcontrol.launch_dependents;");
-  const int pair = blockIdx.x, layer = blockIdx.y;
+  const int pair = blockIdx.x / chunks, chunk = blockIdx.x % chunks, layer = blockIdx.y;
   const int64_t src = __ldg(pairs + 2 * pair), dst = __ldg(pairs + 2 * pair + 1);
   if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
-    if (threadIdx.x == 0 && layer == 0 && blockIdx.z == 0) report(dev_err, PKV_DEV_BAD_BLOCK_ID);
+    if (threadIdx.x == 0 && chunk == 0 && layer == 0 && blockIdx.z == 0)
+      report(dev_err, PKV_DEV_BAD_BLOCK_ID);
     return;
   }
   if (src == dst) return;
   uint4* base = blockIdx.z ? ptrs.v[layer] : ptrs.k[layer];
+  const int64_t lo = chunk * kCopyChunkVecs;
+  const int64_t hi = min(block_vecs, lo + kCopyChunkVecs);
   const uint4* __restrict__ from = base + src * block_vecs;
   uint4* __restrict__ to = base + dst * block_vecs;
-  constexpr int kUnroll = 4;
-  int64_t i = threadIdx.x;
-  for (; i + (kUnroll - 1) * kThreads < block_vecs; i += kUnroll * kThreads) {
-    uint4 r[kUnroll];
+  int64_t i = lo + threadIdx.x;
+  for (; i + (kCopyUnroll - 1) * kThreads < hi; i += kCopyUnroll * kThreads) {
+    uint4 r[kCopyUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) r[u] = __ldg(from + i + u * kThreads);
+    for (int u = 0; u < kCopyUnroll; ++u) r[u] = __ldg(from + i + u * kThreads);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) to[i + u * kThreads] = r[u];
+    for (int u = 0; u < kCopyUnroll; ++u) to[i + u * kThreads] = r[u];
   }
-  for (; i < block_vecs; i += kThreads) to[i] = __ldg(from + i);
+  for (; i < hi; i += kThreads) to[i] = __ldg(from + i);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -155,7 +164,9 @@ extern "C" int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int
   if (block_bytes % 16 != 0) return PKV_ERR_INVALID_ARG;
   if (num_layers == 0 || num_pairs == 0) return PKV_OK;
   if (!k_caches || !v_caches || !block_pairs) return PKV_ERR_INVALID_ARG;
-  if (num_pairs > INT32_MAX) return PKV_ERR_UNSUPPORTED;
+  const int64_t block_vecs = block_bytes / 16;
+  const int64_t chunks = (block_vecs + kCopyChunkVecs - 1) / kCopyChunkVecs;
+  if (static_cast<int64_t>(num_pairs) * chunks > INT32_MAX) return PKV_ERR_UNSUPPORTED;
   for (int base = 0; base < num_layers; base += kMaxLayersPerLaunch) {
     const int n = std::min(kMaxLayersPerLaunch, num_layers - base);
     LayerPtrs ptrs;
@@ -167,8 +178,9 @@ extern "C" int pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int
       ptrs.k[i] = static_cast<uint4*>(kp);
       ptrs.v[i] = static_cast<uint4*>(vp);
     }
-    copy_blocks_kernel<<<dim3(num_pairs, n, 2), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        ptrs, block_pairs, block_bytes / 16, num_blocks, dev_err);
+    copy_blocks_kernel<<<dim3(static_cast<unsigned>(num_pairs * chunks), n, 2), kThreads, 0,
+                         static_cast<cudaStream_t>(stream)>>>(
+        ptrs, block_pairs, block_vecs, static_cast<int>(chunks), num_blocks, dev_err);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
   }
   return PKV_OK;
