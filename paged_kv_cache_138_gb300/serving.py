@@ -2,10 +2,13 @@
 
 Each step is one native call that plans everything on the host (finish, admit
 with prefix-cache hits, append a sampled token per running request, preempt by
-recompute or swap, copy-on-write, tables), followed by the device work it
-returns, in order: swap-ins and prefill writes, swap-outs, copy_blocks, the
-new tokens' reshape_and_cache and paged attention over the batch.  Python only
-marshals the arrays and launches the kernels.
+recompute or swap, copy-on-write, tables, shared-prefix groups), followed by
+the device work it returns, in order: swap-ins and prefill writes, swap-outs,
+copy_blocks, then one fused launch that writes the new tokens' K/V and runs
+paged attention over the batch (grouped when the step formed groups), and the
+merge.  The step's metadata and prefill slots are copied on a side stream
+while the previous step's kernels run; the decode stream waits only for that
+copy.  Python only marshals the arrays and launches.
 
 Values (K/V of prefill and decoded tokens, queries) come from a source object:
 ``DeviceRandomValues`` draws them on the device (benchmarks);
