@@ -19,6 +19,8 @@ synthetic, there is no dataset):
                      32 heads MHA
   llama2-7b-32layer  32 layers x 64 sequences x 4096 tokens, 32 heads MHA, one
                      table shared by all layers over 16384 blocks per layer
+  llama2-7b-layer    one layer of that step (same shapes, 4 GiB of K+V): small
+                     enough to profile where the 128 GiB step is not
 
 Common: head_dim 128, block_size 16, q/K/V ~ N(0, 1) rounded to fp16, the new
 token counted in the context length L (it is written at position L - 1 before
@@ -65,6 +67,8 @@ WORKLOADS = {
                                description="8 prompts x 2048 tok forked x16, +64..512 private tok"),
     "llama2-7b-32layer": Workload("llama2-7b-32layer", 5, 64, 32, 32, num_layers=32,
                                   description="Llama-2-7B full step, 32 layers, batch 64 x 4096"),
+    "llama2-7b-layer": Workload("llama2-7b-layer", 6, 64, 32, 32,
+                                description="one layer of the Llama-2-7B step, batch 64 x 4096"),
 }
 
 
@@ -84,7 +88,7 @@ def context_lengths(w: Workload) -> np.ndarray:
         return np.array([7, 16, 31, 48, 63], dtype=np.int32)
     if w.name == "llama2-13b-layer":
         return rng.integers(1, 4096, size=w.num_seqs, endpoint=True).astype(np.int32)
-    if w.name in ("gqa-32-8", "llama2-7b-32layer"):
+    if w.name in ("gqa-32-8", "llama2-7b-32layer", "llama2-7b-layer"):
         return np.full(w.num_seqs, 4096, dtype=np.int32)
     if w.name == "prefix-sharing":
         p = prefix_sharing_private_tokens(w)
@@ -96,7 +100,7 @@ def pool_blocks(w: Workload, lengths: Optional[np.ndarray] = None) -> int:
     """Physical blocks in the pool for workload ``w``."""
     if w.name == "tiny" and w.block_size == BLOCK_SIZE:
         return 64
-    if w.name == "llama2-7b-32layer":
+    if w.name in ("llama2-7b-32layer", "llama2-7b-layer"):
         return w.num_seqs * blocks_for(4096, w.block_size)
     if w.name == "prefix-sharing":
         p = prefix_sharing_private_tokens(w)
