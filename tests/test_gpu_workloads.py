@@ -90,6 +90,10 @@ def test_llama2_7b_32_layer_full_size(native_lib):
     run_and_check("llama2-7b-32layer", [0, 31], 96)
 
 
+def test_llama2_7b_single_layer_full_size(native_lib):
+    run_and_check("llama2-7b-layer", [0], 128)
+
+
 def test_llama2_7b_every_layer_sampled(native_lib):
     """All 32 layers of the 7B step.  Per layer a few sequences are drawn and
     only their blocks are copied to the host before the step (compacted,
