@@ -46,6 +46,10 @@ class BlockManager:
         return check(rc, what)
 
     def allocate(self, seq, tokens):
+        """Blocks for a new sequence's prompt: the physical block table (list of
+        ints).  Leading full blocks found in the prefix cache (at most
+        (len - 1) // block_size of them) are reused; raises OutOfBlocks with
+        the state unchanged when the pool cannot hold the rest."""
         toks = _i32(tokens)
         cap = -(-len(toks) // self.block_size)
         table = np.empty(max(cap, 1), dtype=np.int32)
@@ -56,6 +60,10 @@ class BlockManager:
         return table[:nt.value].tolist()
 
     def append_slot(self, seq, token):
+        """Append one token: the slot (block * block_size + offset) it goes to.
+        Takes a new block when the last is full, or a private copy of a shared
+        last block (copy-on-write, pair queued for take_cow_pairs); raises
+        OutOfBlocks with the state unchanged."""
         slot = ctypes.c_int64()
         self._check(lib().pkv_bm_append_slot(self._h, int(seq), int(token), ctypes.byref(slot)),
                     "append_slot")
@@ -85,18 +93,23 @@ class BlockManager:
         return slots, int(done.value), int(rc)
 
     def fork(self, parent, child):
+        """child shares every block of parent (reference counts + 1)."""
         self._check(lib().pkv_bm_fork(self._h, int(parent), int(child)), "fork")
 
     def free(self, seq):
+        """Release a sequence's blocks, last first: hashed blocks whose count
+        drops to 0 join the evictable pool, the others the free list."""
         self._check(lib().pkv_bm_free(self._h, int(seq)), "free")
 
     def slot(self, seq, pos):
+        """table[pos // block_size] * block_size + pos % block_size."""
         out = ctypes.c_int64()
         self._check(lib().pkv_bm_slot(self._h, int(seq), int(pos), ctypes.byref(out)), "slot")
         return out.value
 
     @property
     def num_free_blocks(self):
+        """Blocks an allocation may take: the free list plus the evictable pool."""
         return int(lib().pkv_bm_num_free_blocks(self._h))
 
     @property
@@ -110,9 +123,12 @@ class BlockManager:
         return 1.0 - self.num_free_blocks / self.num_blocks
 
     def can_allocate(self, num_tokens):
+        """The coarse check ceil(num_tokens / block_size) <= num_free_blocks
+        (prefix-cache hits not counted)."""
         return bool(lib().pkv_bm_can_allocate(self._h, int(num_tokens)))
 
     def block_table(self, seq):
+        """The sequence's physical block ids, logical order."""
         n = lib().pkv_bm_block_table(self._h, int(seq), None, 0)
         if n < 0:
             raise PagedKVError(int(n), "block_table")
@@ -121,12 +137,15 @@ class BlockManager:
         return out[:n].tolist()
 
     def num_tokens(self, seq):
+        """Tokens the sequence holds (prompt + appended)."""
         n = lib().pkv_bm_num_tokens(self._h, int(seq))
         if n < 0:
             raise PagedKVError(int(n), "num_tokens")
         return int(n)
 
     def num_cached_tokens(self, seq):
+        """Prompt tokens its allocate found in the prefix cache (a multiple of
+        block_size)."""
         n = lib().pkv_bm_num_cached_tokens(self._h, int(seq))
         if n < 0:
             raise PagedKVError(int(n), "num_cached_tokens")
@@ -146,6 +165,8 @@ class BlockManager:
         return tables, lens
 
     def take_cow_pairs(self):
+        """The (src, dst) block pairs queued by copy-on-write appends since the
+        last call, for copy_blocks; the queue is emptied."""
         n = lib().pkv_bm_take_cow_pairs(self._h, None, 0)
         out = np.empty((max(n, 1), 2), dtype=np.int64)
         lib().pkv_bm_take_cow_pairs(self._h, _p(out), n)

@@ -17,6 +17,11 @@ from .scenario import DecodeBatch
 
 
 class DecodeStep:
+    """One decode batch resident in HBM (caches of every layer, the step's
+    inputs, output and workspace) and the launches of one step over it:
+    eager (prepared launches), from a CUDA graph, or fed from pinned host
+    buffers (sequential or pipelined)."""
+
     def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None,
                  fused=False, grouped=False):
         """host_values: None draws q/K/V on the device (torch generator seeded by
@@ -132,6 +137,7 @@ class DecodeStep:
         self._prepared("attend", i, stream, b, make)()
 
     def run(self, stream=None, bufs=None):
+        """Every layer of one step (without the COW copies: apply_cow)."""
         for i in range(self.num_layers):
             self.run_layer(i, stream, bufs)
         return self.out if bufs is None else bufs.out
@@ -156,10 +162,12 @@ class DecodeStep:
         return g
 
     def replay(self):
+        """Launch the captured step (capture_graph) with one call."""
         self.graph.replay()
         return self.out
 
     def kernel_launches_per_step(self):
+        """Kernels of this library one run() launches (COW copies excluded)."""
         merge = 1 if ops.workspace_bytes(self.batch.num_seqs, self.q.shape[2],
                                          self.batch.max_blocks,
                                          self.batch.workload.block_size) else 0
@@ -168,6 +176,7 @@ class DecodeStep:
         return self.num_layers * ((1 if self.fused else 2) + merge)
 
     def check_errors(self):
+        """Synchronise and raise if a kernel reported a device error code."""
         code = ops.read_error_word(self.dev_err)
         if code:
             raise RuntimeError("device reported error code %d" % code)
@@ -186,12 +195,15 @@ class DecodeStep:
         return self._host
 
     def host_bytes_per_step(self):
+        """(host-to-device, device-to-host) bytes of one step fed from host."""
         h = self.host_buffers()
         up = sum(h[k].numel() * h[k].element_size()
                  for k in ("q", "k_new", "v_new", "slot_mapping", "block_tables", "context_lens"))
         return up, h["out"].numel() * h["out"].element_size()
 
     def run_from_host(self, stream=None):
+        """One step whose inputs come from pinned host buffers and whose output
+        goes back to one (the copies on the step's stream)."""
         h = self.host_buffers()
         s = torch.cuda.current_stream() if stream is None else stream
         with torch.cuda.stream(s):

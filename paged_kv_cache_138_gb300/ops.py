@@ -90,6 +90,8 @@ def read_error_word(dev_err):
 
 def workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size=BLOCK_SIZE,
                     head_dim=HEAD_DIM):
+    """Bytes of split-K partials paged_attention_decode may need (an upper
+    bound over the split lengths a launch of these sizes can choose)."""
     return int(lib().pkv_paged_attention_workspace_bytes(num_seqs, num_q_heads,
                                                          max_blocks_per_seq, block_size,
                                                          head_dim))
@@ -106,6 +108,7 @@ def split_tokens(num_seqs, num_kv_heads, max_blocks_per_seq, block_size=BLOCK_SI
 
 def alloc_workspace(num_seqs, num_q_heads, max_blocks_per_seq, device=None,
                     block_size=BLOCK_SIZE):
+    """A device buffer of workspace_bytes (None when no split is possible)."""
     n = workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, block_size)
     if n == 0:
         return None
@@ -294,6 +297,8 @@ def shared_prefix_groups(block_tables, context_lens, block_size=BLOCK_SIZE, grou
 
 def grouped_workspace_bytes(num_seqs, num_q_heads, max_blocks_per_seq, max_shared_tokens,
                             block_size=BLOCK_SIZE, head_dim=HEAD_DIM):
+    """Workspace bytes of the grouped entry points: the split-K bound plus the
+    partial slots of shared prefixes up to max_shared_tokens."""
     return int(lib().pkv_paged_attention_grouped_workspace_bytes(
         num_seqs, num_q_heads, max_blocks_per_seq, block_size, head_dim, max_shared_tokens))
 

@@ -61,6 +61,13 @@ class _DecodeLaunch(ctypes.Structure):
 
 
 class NativeServingDriver:
+    """Continuous batching without a model: the native scheduler plans each
+    step on a BlockManager (admissions with prefix-cache hits, one sampled
+    token per running request, preemption by recompute or swap, copy-on-write,
+    shared-prefix groups) and step() launches the device work it returns.
+    K/V and q values come from ``values`` (DeviceRandomValues or
+    ContentKeyedValues)."""
+
     def __init__(self, num_blocks, num_q_heads, num_kv_heads, max_batch, max_blocks_per_seq,
                  values, device="cuda", block_size=16, head_dim=128, enable_prefix_cache=True,
                  free_order=None, preemption="recompute", host_blocks=0, seed=0, grouped=False):
@@ -186,6 +193,7 @@ class NativeServingDriver:
             self._h = None
 
     def add_request(self, rid, prompt, max_new_tokens):
+        """Queue a request: prompt token ids, tokens to generate."""
         p = np.ascontiguousarray(prompt, dtype=np.int32)
         rc = lib().pkv_sched_add_request(self._h, int(rid), p.ctypes.data_as(ctypes.c_void_p),
                                          len(p), int(max_new_tokens))
@@ -194,9 +202,11 @@ class NativeServingDriver:
 
     @property
     def idle(self):
+        """True when no request is waiting or running."""
         return lib().pkv_sched_num_unfinished(self._h) == 0
 
     def request_tokens(self, rid):
+        """A request's tokens so far (prompt + generated), int32."""
         n = lib().pkv_sched_request_tokens(self._h, int(rid), None, 0)
         if n < 0:
             raise PagedKVError(int(n), "request_tokens")
@@ -293,6 +303,7 @@ class NativeServingDriver:
         return res
 
     def check_errors(self):
+        """Synchronise and raise if a kernel reported a device error code."""
         code = ops.read_error_word(self.dev_err)
         if code:
             raise RuntimeError("device reported error code %d" % code)
