@@ -227,8 +227,7 @@ class DecodeStep:
             ev = lambda: torch.cuda.Event()
             self._pipe = SimpleNamespace(
                 sets=sets, copy=torch.cuda.Stream(self.device),
-                inputs_ready=[ev(), ev()], compute_done=[ev(), ev()], out_copied=[ev(), ev()],
-                started=[False, False])
+                inputs_ready=[ev(), ev()], compute_done=[ev(), ev()], started=[False, False])
         return self._pipe
 
     def run_from_host_pipelined(self, host_inputs, host_outputs, stream=None):
@@ -259,9 +258,10 @@ class DecodeStep:
             b = P.sets[j]
             if k + 1 < n:
                 upload(k + 1)
+            # the copy stream runs in order and took step k's inputs after step
+            # k-2's output copy (uploads of k+1 are enqueued after the output
+            # copy of k-1), so this one wait also covers set j's out buffer
             s.wait_event(P.inputs_ready[j])
-            if P.started[j]:
-                s.wait_event(P.out_copied[j])              # step k-2's output is on the host
             self.apply_cow(s)
             self.run(s, bufs=b)
             P.compute_done[j].record(s)
@@ -269,5 +269,4 @@ class DecodeStep:
             with torch.cuda.stream(P.copy):
                 P.copy.wait_event(P.compute_done[j])
                 host_outputs[k].copy_(b.out, non_blocking=True)
-                P.out_copied[j].record(P.copy)
         return host_outputs
