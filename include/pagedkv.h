@@ -287,7 +287,8 @@ int pkv_slot_mapping(const int32_t* block_tables, const int32_t* positions, int 
  * writes into a block it still shares after a fork, it takes a new block and
  * the old block's KV is copied into it (the page copies the valid bytes; the
  * whole block is copied here, so dst equals src byte for byte).
- *   k_caches, v_caches  HOST arrays of num_layers device pointers (1..64 layers)
+ *   k_caches, v_caches  HOST arrays of num_layers device pointers (one launch per
+ *                64 layers)
  *   block_pairs  int64 [num_pairs, 2] (device), (src, dst) per row; ids outside
  *                [0, num_blocks) are skipped and reported as PKV_DEV_BAD_BLOCK_ID
  *   block_bytes  bytes of one block of one cache (16 * num_kv_heads * head_dim * 2

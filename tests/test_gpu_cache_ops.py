@@ -113,6 +113,27 @@ def test_copy_blocks_multi_layer_and_bad_pair(ops):
         assert np.array_equal(bits(d), a.view(np.uint16))
 
 
+@pytest.mark.parametrize("Hkv", [12, 40])
+def test_copy_blocks_partial_last_chunk(ops, Hkv):
+    """A block copy is cut into 32 KB chunks: 12 KV heads make 48 KB blocks (a
+    full chunk and half of one), 40 make 160 KB (five); every other block
+    stays as it was."""
+    rng = np.random.default_rng(Hkv)
+    shape = (24, 16, Hkv, 128)
+    kc = rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    vc = rng.standard_normal(shape, dtype=np.float32).astype(np.float16)
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    # destinations are fresh blocks, as copy-on-write makes them (no pair
+    # writes a block another pair reads)
+    pairs = np.array([[0, 23], [5, 6], [11, 11], [17, 1], [2, 20]], dtype=np.int64)
+    err = ops.new_error_word()
+    ops.copy_blocks(dk, dv, torch.from_numpy(pairs).cuda(), dev_err=err)
+    assert ops.read_error_word(err) == 0
+    oc.copy_blocks([kc], [vc], pairs)
+    assert np.array_equal(bits(dk), kc.view(np.uint16))
+    assert np.array_equal(bits(dv), vc.view(np.uint16))
+
+
 def test_swap_blocks_device_host_round_trip(ops):
     """swap-out to pinned host memory and swap-in to other device blocks, bit-exact
     against the oracle's copy definition."""
