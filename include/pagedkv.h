@@ -363,6 +363,7 @@ typedef struct pkv_block_manager pkv_block_manager;
  * order in which free blocks are handed out).  Returns NULL on bad arguments. */
 pkv_block_manager* pkv_bm_create(int64_t num_blocks, int block_size, int enable_prefix_cache,
                                  const int32_t* initial_free_order);
+/* Frees the manager (NULL is ignored). */
 void pkv_bm_destroy(pkv_block_manager* bm);
 
 /* Allocate a new sequence holding num_tokens prompt tokens.  Writes its block
@@ -390,13 +391,18 @@ int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
 /* Release a sequence (unknown ids are ignored; never fails). */
 int pkv_bm_free(pkv_block_manager* bm, int64_t seq_id);
 
+/* Slot of position pos ("P06 BlockManager": table[pos / bs] * bs + pos % bs);
+ * PKV_ERR_BAD_INDEX for an unknown id, a negative position or one past its table. */
 int pkv_bm_slot(const pkv_block_manager* bm, int64_t seq_id, int64_t pos, int64_t* slot_out);
+/* Blocks an allocation may take: free list + evictable pool. */
 int64_t pkv_bm_num_free_blocks(const pkv_block_manager* bm);
 /* The coarse check ceil(num_tokens / bs) <= num_free_blocks: 1 or 0. */
 int pkv_bm_can_allocate(const pkv_block_manager* bm, int64_t num_tokens);
 /* Table length of a sequence (or PKV_ERR_BAD_INDEX); copies up to cap entries. */
 int64_t pkv_bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t* out, int64_t cap);
+/* Tokens a sequence holds (prompt + appended), or PKV_ERR_BAD_INDEX. */
 int64_t pkv_bm_num_tokens(const pkv_block_manager* bm, int64_t seq_id);
+/* Prompt tokens its allocate found in the prefix cache, or PKV_ERR_BAD_INDEX. */
 int64_t pkv_bm_num_cached_tokens(const pkv_block_manager* bm, int64_t seq_id);
 /* Rows [n, max_blocks] of block tables (pad entries past each table) and the
  * token counts of the listed sequences, ready for the attention kernel. */
@@ -470,6 +476,7 @@ typedef struct pkv_sched_step_out {
 pkv_scheduler* pkv_sched_create(pkv_block_manager* bm, int max_batch, int max_blocks_per_seq,
                                 int block_size, int preemption_swap, int64_t host_blocks,
                                 uint64_t seed, int vocab);
+/* Frees the scheduler (not its BlockManager; NULL is ignored). */
 void pkv_sched_destroy(pkv_scheduler* sched);
 /* Queue a request (ids unique; prompt non-empty; prompt + max_new_tokens must
  * fit max_blocks_per_seq blocks). */
