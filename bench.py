@@ -6,53 +6,70 @@
 
 A step is one decode step of the workload: (copy_blocks for pending
 copy-on-write pairs,) then per layer reshape_and_cache of the new token and
-paged decode attention over every sequence.  Inputs are synthetic and resident
-in HBM before timing starts.  The default workload is the Llama-2-13B layer
-shape: batch 64, context lengths ~ U[1, 4096], 40 heads MHA, head_dim 128,
-block_size 16 (KV of one step ~2.7 GB, far larger than the 129 MB L2, so no
-flush is needed between steps).  A workload whose step would fit in 4x the L2
-size (the 5-sequence tiny case) is timed step by step instead, each step
-between its own events and L2 flushed by a buffer write after each.
+paged decode attention over every sequence (one fused launch per layer by
+default).  Inputs are synthetic and resident in HBM before timing starts.  The
+default workload is the full Llama-2-7B decode step at batch 64 x 4096-token
+contexts: 32 layers x 32 heads MHA, head_dim 128, block_size 16, blocks
+scattered over a 128 GiB K+V pool (137 GB of KV read per step, far larger than
+the 129 MB L2, so no flush is needed between steps).  A workload whose step
+would fit in 4x the L2 size (the 5-sequence tiny case) is timed step by step
+instead, each step between its own events and L2 flushed by a buffer write
+after each.
 
 Prints one JSON line.  `value` is KV bytes read per step / device time per step
 (GB/s, whole job over all ranks); `e2e` is the same metric through the same
 public API with the step inputs copied from pinned host memory and the output
-copied back inside the timed region.  `--impl reference` times the CPU fp64
-oracle on the host cores instead (bounded samples of the same workload).
-Under torchrun each rank runs its own copy of the batch (weak scaling, no
-collective on the data path).
+copied back inside the timed region; `roofline` times the attention launch
+alone in a loop of its own.  `--impl reference` times the CPU fp64 oracle on
+the host cores instead, on bounded samples of the same workload whose inputs
+it draws itself (no GPU code runs in that arm).  Under torchrun each rank runs
+its own copy of the batch (weak scaling, no collective on the data path).
 """
 import argparse
+import dataclasses
+import datetime
 import json
 import os
 import statistics
 import subprocess
 import sys
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-E2E_CHUNKS = 5
-# the attention launch is bracketed by its own CUDA events on every
-# ATTN_SAMPLE_EVERY-th timed step: each timing event costs ~2 us of device
-# time, which on every step would lengthen the step being measured
-ATTN_SAMPLE_EVERY = 16
+DEFAULT_WORKLOAD = "llama2-7b-32layer"
+DECODE_WORKLOADS = ("tiny", "llama2-13b-layer", "gqa-32-8", "prefix-sharing",
+                    "llama2-7b-32layer", "llama2-7b-layer")
+# end-to-end windows: fixed sizes, whatever --steps is, so that the one
+# unoverlapped upload at a window's start and download at its end are spread
+# over enough pipelined steps
+E2E_WINDOWS = 5
+E2E_STEPS_PER_WINDOW = 50
+# the attention launch alone: this many back-to-back launches between two events
+ROOFLINE_LAUNCHES = 200
+CLOCK_PERIOD_MS = 50
+# sequences per sample of the oracle arm (one layer, every head of each)
+REFERENCE_SAMPLE_SEQS = 8
 METRIC = "paged decode attention KV GB/s (% of GB300 HBM peak) and seq-steps/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama2-13b-layer")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(DECODE_WORKLOADS) + ["serving", "swap"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=None,
+                    help="pipelined steps per end-to-end window (default %d)"
+                         % E2E_STEPS_PER_WINDOW)
     ap.add_argument("--unfused", action="store_true",
                     help="separate reshape_and_cache and attention launches per layer")
     ap.add_argument("--driver", choices=["native", "python"], default="native",
@@ -61,7 +78,7 @@ def parse():
                     help="shared-prefix grouped attention (auto: on for prefix-sharing)")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per KV block: 8, 16, 32 or 64")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -108,165 +125,286 @@ def traffic_record(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+    """nvidia-smi samples of SM clock and throttle reasons, each stamped with
+    nvidia-smi's own wall-clock timestamp, so that the samples taken inside a
+    timed region can be picked out afterwards (the tool's pipe output arrives
+    in bursts, so arrival times say nothing)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.idx = gpu_index
-        self.proc = None
+    def __init__(self, gpu_index, period_ms=CLOCK_PERIOD_MS):
+        self.idx, self.period_ms = gpu_index, period_ms
+        self.proc, self.samples, self.t_start = None, [], None
+        self._lines, self._reader = [], None
 
-    def __enter__(self):
+    def start(self):
+        self.t_start = time.time()
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
         except Exception:
             self.proc = None
         return self
 
-    def __exit__(self, *exc):
-        self.lines = []
+    def _read(self):
+        for line in self.proc.stdout:
+            self._lines.append(line)
+
+    def ready(self, settle_s=0.6):
+        """Wait until the tool has been sampling for settle_s."""
         if self.proc is not None:
+            time.sleep(max(0.0, self.t_start + settle_s - time.time()))
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(2.0 * self.period_ms / 1e3)
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
-
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in getattr(self, "lines", []):
+            if self._reader is not None:
+                self._reader.join(timeout=5)
+        self.samples = []
+        for line in self._lines:
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, mx = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            reasons = {n for n, v in zip(self.REASONS, f[6:10]) if v.lower().startswith("active")}
+            self.samples.append((ts, sm, mx, reasons))
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and the throttle reasons seen, over the
+        samples stamped in [t0, t1] (all samples when no window is given)."""
+        sel = [s for s in self.samples
+               if (t0 is None or s[0] >= t0) and (t1 is None or s[0] <= t1)]
+        sm = [s[1] for s in sel]
+        reasons = set().union(*[s[3] for s in sel]) if sel else set()
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": sel[-1][2] if sel else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "period_ms": self.period_ms}
 
 
-def cpu_oracle_sample(step, layer, seqs, heads, min_seconds=0.0, threads=None):
-    """Time the fp64 oracle on a sample of sequences of one layer (host cores,
-    or ``threads`` of them), repeating the sample until at least
-    ``min_seconds`` of oracle time.
-    Returns (seconds, KV bytes attended over in that time, threads)."""
-    import numpy as np
-
-    from oracle import attention as oa
-    from oracle import cache_ops as oc
+def workload_config(w, tables, lens, num_blocks, l2_bytes):
+    """The `config` object of the JSON line: the workload's shape and sizes,
+    from host metadata only (both arms print the same one)."""
     from paged_kv_cache_138_gb300 import accounting
+    kv = accounting.step_kv_bytes(lens, w.num_kv_heads, w.head_dim, layers=w.num_layers)
+    unique = None
+    if w.name == "prefix-sharing":
+        unique = accounting.unique_kv_bytes(tables, lens, w.block_size, w.num_kv_heads,
+                                            w.head_dim)
+    step_bytes = unique if unique is not None else kv / w.num_layers
+    alloc = sum(-(-int(L) // w.block_size) * w.block_size for L in lens)
+    cfg = {"workload": w.name, "description": w.description,
+           "num_seqs": int(len(lens)), "num_q_heads": w.num_q_heads,
+           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+           "block_size": w.block_size, "layers": w.num_layers,
+           "tokens": int(sum(int(L) for L in lens)), "kv_bytes_per_step": kv,
+           "unique_kv_bytes_per_step": unique, "pool_blocks": int(num_blocks),
+           "tail_waste_pct": 100.0 * (alloc - sum(int(L) for L in lens)) / alloc}
+    if l2_bytes is None:
+        cfg["l2"] = "unknown L2 size (no GPU)"
+    elif step_bytes < 4 * l2_bytes:
+        cfg["l2"] = ("L2 flushed between timed steps (%d MiB write, outside the per-step "
+                     "events)" % (max(4 * l2_bytes, 512 << 20) >> 20))
+    else:
+        cfg["l2"] = ("inputs larger than L2 (%.0f MB per layer-step vs %.0f MB L2); no flush"
+                     % (step_bytes / 1e6, l2_bytes / 1e6))
+    return cfg, kv, unique
 
-    b = step.batch
-    w = b.workload
-    tables = b.block_tables[seqs]
-    lens = b.context_lens[seqs]
-    blocks = sorted({int(x) for row, L in zip(tables, lens) for x in row[:(int(L) + 15) // 16]})
-    remap = {blk: i for i, blk in enumerate(blocks)}
+
+def device_l2_bytes():
     import torch
-    idx = torch.tensor(blocks, dtype=torch.long, device=step.k_cache.device)
-    kc = step.k_cache[layer].index_select(0, idx).cpu().numpy()
-    vc = step.v_cache[layer].index_select(0, idx).cpu().numpy()
-    t2 = np.array([[remap.get(int(x), -1) if x >= 0 else -1 for x in row] for row in tables],
-                  dtype=np.int32)
-    slots = np.array([remap[int(s) // 16] * 16 + int(s) % 16 for s in b.slot_mapping[seqs]],
-                     dtype=np.int64)
-    q = step.q[layer].cpu().numpy()[seqs]
-    kn = step.k_new[layer].cpu().numpy()[seqs]
-    vn = step.v_new[layer].cpu().numpy()[seqs]
-    si = np.repeat(np.arange(len(seqs), dtype=np.int32), len(heads))
-    hi = np.tile(np.array(heads, dtype=np.int32), len(seqs))
-    frac_heads = len(heads) / w.num_q_heads
-    kv_once = accounting.step_kv_bytes(lens, w.num_kv_heads, w.head_dim) * frac_heads
-    dt, kv = 0.0, 0.0
-    all_threads = oa.num_threads()
-    if threads is not None:
-        oa.set_num_threads(threads)
-    try:
-        while True:
-            t0 = time.perf_counter()
-            oc.reshape_and_cache(kn, vn, slots, kc, vc)
-            oa.paged_attention_decode_rows(q, kc, vc, t2, lens, w.scale, si, hi)
-            dt += time.perf_counter() - t0
-            kv += kv_once
-            if dt >= min_seconds:
-                return dt, kv, oa.num_threads()
-    finally:
-        oa.set_num_threads(all_threads)
+    if not torch.cuda.is_available():
+        return None
+    return torch.cuda.get_device_properties(0).L2_cache_size
 
 
-def setup(args, device, rank=0):
+def bench_workload(args, rank=0):
     from paged_kv_cache_138_gb300 import dist as pd
     from paged_kv_cache_138_gb300 import workloads as wl
-    from paged_kv_cache_138_gb300.engine import DecodeStep
-    from paged_kv_cache_138_gb300.scenario import prepare_batch
-    import dataclasses
     w = pd.replica(wl.WORKLOADS[args.workload], rank)
     if args.block_size != w.block_size:
         if args.workload == "prefix-sharing":
             raise SystemExit("the prefix-sharing workload is defined for block size 16")
         w = dataclasses.replace(w, block_size=args.block_size)
-    batch = prepare_batch(w)
-    grouped = {"on": True, "off": False}.get(getattr(args, "grouped", "auto"),
-                                              args.workload == "prefix-sharing")
-    step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False),
-                      grouped=grouped)
-    return w, batch, step
+    return w
+
+
+class OracleSampler:
+    """Times the fp64 C oracle -- reshape_and_cache of the new token, then
+    attention over every head of one layer -- on a few sequences of the
+    workload.  Its inputs are drawn here on the host (seeded N(0, 1) fp16 for
+    q, the new K/V and the K/V of the sequences' blocks, compacted into a small
+    pool), from the oracle's own batch metadata: nothing of the GPU path is
+    used.  Timing depends on the shapes and lengths only, not on the values."""
+
+    def __init__(self, w, tables, lens, max_seqs, seed):
+        import numpy as np
+
+        from paged_kv_cache_138_gb300 import workloads as wl
+        self.w, self.tables, self.lens = w, tables, lens
+        bs = w.block_size
+        per_seq = sorted(-(-int(L) // bs) for L in lens)
+        cap = max(1, sum(per_seq[-max_seqs:]))
+        rng = np.random.default_rng([seed, 99])
+        shape = (cap, bs, w.num_kv_heads, w.head_dim)
+        self.kc = wl.host_normal_fp16(rng, shape)
+        self.vc = wl.host_normal_fp16(rng, shape)
+        self.q = wl.host_normal_fp16(rng, (max_seqs, w.num_q_heads, w.head_dim))
+        self.k_new = wl.host_normal_fp16(rng, (max_seqs, w.num_kv_heads, w.head_dim))
+        self.v_new = wl.host_normal_fp16(rng, (max_seqs, w.num_kv_heads, w.head_dim))
+
+    def time(self, seqs, min_seconds=0.0, threads=None):
+        """(seconds, KV bytes attended over in that time, threads used): the
+        sample repeated until at least min_seconds of oracle time."""
+        import numpy as np
+
+        from oracle import attention as oa
+        from oracle import cache_ops as oc
+        from paged_kv_cache_138_gb300 import accounting
+        w, bs = self.w, self.w.block_size
+        lens = np.ascontiguousarray(self.lens[seqs], dtype=np.int32)
+        remap = {}
+        rows = []
+        for s, L in zip(seqs, lens):
+            ids = [int(b) for b in self.tables[s][:-(-int(L) // bs)]]
+            rows.append([remap.setdefault(b, len(remap)) for b in ids])
+        t2 = np.full((len(seqs), max(len(r) for r in rows)), -1, dtype=np.int32)
+        for i, r in enumerate(rows):
+            t2[i, :len(r)] = r
+        # the new token of each sequence sits at position L - 1 (the slot rule)
+        slots = np.array([oc.slot(t2[i], int(L) - 1, bs) for i, L in enumerate(lens)],
+                         dtype=np.int64)
+        n = len(seqs)
+        q, kn, vn = self.q[:n], self.k_new[:n], self.v_new[:n]
+        si = np.repeat(np.arange(n, dtype=np.int32), w.num_q_heads)
+        hi = np.tile(np.arange(w.num_q_heads, dtype=np.int32), n)
+        kv_once = accounting.step_kv_bytes(lens, w.num_kv_heads, w.head_dim)
+        dt, kv = 0.0, 0.0
+        all_threads = oa.num_threads()
+        if threads is not None:
+            oa.set_num_threads(threads)
+        try:
+            while True:
+                t0 = time.perf_counter()
+                oc.reshape_and_cache(kn, vn, slots, self.kc, self.vc)
+                oa.paged_attention_decode_rows(q, self.kc, self.vc, t2, lens, w.scale, si, hi)
+                dt += time.perf_counter() - t0
+                kv += kv_once
+                if dt >= min_seconds:
+                    return dt, kv, oa.num_threads()
+        finally:
+            oa.set_num_threads(all_threads)
+
+
+def oracle_metadata(w):
+    """The oracle's own batch (tables, lengths, slots, COW pairs, pool size)."""
+    from oracle.batch import oracle_batch
+    return oracle_batch(w)
+
+
+def cpu_baseline(w, tables, lens):
+    """The oracle on the host cores: 8 random sequences x every head of layer 0
+    for ~10 s with every core, and 2 of them on one core for ~3 s."""
+    import numpy as np
+    from oracle.build import build_oracle
+    build_oracle()
+    S = len(lens)
+    seqs = sorted(np.random.default_rng(3).choice(S, size=min(S, REFERENCE_SAMPLE_SEQS),
+                                                  replace=False).tolist())
+    smp = OracleSampler(w, tables, lens, len(seqs), seed=w.seed)
+    tot_t, tot_kv, threads = smp.time(seqs, min_seconds=10.0)
+    cpu = {"value": tot_kv / tot_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": "%d random of %d sequences x all %d heads of layer 0 (reshape_and_cache "
+                     "+ attention), repeated for %.1f s (fp64 C oracle, OpenMP; host-drawn "
+                     "inputs)" % (len(seqs), S, w.num_q_heads, tot_t)}
+    t1, kv1, _ = smp.time(seqs[:2], min_seconds=3.0, threads=1)
+    cpu["single_thread"] = {"value": kv1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
+                            "sample": "%d sequences x all %d heads, repeated for %.1f s" % (
+                                min(2, len(seqs)), w.num_q_heads, t1)}
+    return cpu
 
 
 def run_reference(args):
-    """The reference arm: the CPU fp64 oracle, timed on this host's cores."""
+    """The reference arm: the CPU fp64 oracle, timed on this host's cores, on
+    bounded samples of the same workload.  It loads no GPU code of this
+    repository: metadata from the oracle's BlockManager, values drawn on the
+    host, the oracle's C library."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
+    if args.workload not in DECODE_WORKLOADS:
+        print(json.dumps({"impl": "reference", "unavailable":
+                          "no oracle arm for the %s workload" % args.workload}))
+        return 0
+    l2 = device_l2_bytes()
+    if l2 is None:
+        print(json.dumps({"impl": "reference",
+                          "unavailable": "no CUDA device: the workload's L2 rule needs it"}))
+        return 0
     import numpy as np
-    import torch
-
     from oracle.build import build_oracle
     build_oracle()
-    device = "cuda:0" if torch.cuda.is_available() else "cpu"
-    if device == "cpu":
-        print(json.dumps({"impl": "reference", "unavailable": "no CUDA device to hold the workload"}))
-        return 0
-    from paged_kv_cache_138_gb300 import build as nb
-    nb.build()
-    w, batch, step = setup(args, device)
-    S = batch.num_seqs
+    w = bench_workload(args)
+    tables, lens, _, _, nb = oracle_metadata(w)
+    cfg, kv_step, _ = workload_config(w, tables, lens, nb, l2)
+    S = len(lens)
+    n = min(S, REFERENCE_SAMPLE_SEQS)
+    smp = OracleSampler(w, tables, lens, n, seed=w.seed)
     rng = np.random.default_rng(5)
-    heads = list(range(w.num_q_heads))
     times, kvs, threads = [], [], 1
     for i in range(args.warmup + args.steps):
-        seqs = sorted(rng.choice(S, size=min(2, S), replace=False).tolist())
-        dt, kv, threads = cpu_oracle_sample(step, 0, seqs, heads)
+        seqs = sorted(rng.choice(S, size=n, replace=False).tolist())
+        dt, kv, threads = smp.time(seqs)
         if i >= args.warmup:
             times.append(dt)
             kvs.append(kv)
     value = sum(kvs) / sum(times) / 1e9
-    sample = "%d steps, each 2 random sequences x all %d heads of 1 layer (fp64 oracle)" % (
-        args.steps, w.num_q_heads)
+    sample = ("%d steps, each %d random of %d sequences x all %d heads of one layer "
+              "(fp64 oracle; host-drawn inputs)" % (args.steps, n, S, w.num_q_heads))
+    ms_full = 1e3 * kv_step / (value * 1e9)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "ms_per_step": ms_full, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "description": w.description},
+            "config": cfg,
+            "ms_per_step_note": "a full step of the workload (%d layers x %d sequences) at "
+                                "the sampled rate; each timed sample took %.2f ms on average"
+                                % (w.num_layers, S, 1e3 * sum(times) / len(times)),
+            "seq_steps_per_s": world * S / (ms_full / 1e3),
             "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
+
+
+def setup(args, device, rank=0):
+    from paged_kv_cache_138_gb300.engine import DecodeStep
+    from paged_kv_cache_138_gb300.scenario import prepare_batch
+    w = bench_workload(args, rank)
+    batch = prepare_batch(w)
+    grouped = {"on": True, "off": False}.get(getattr(args, "grouped", "auto"),
+                                              args.workload == "prefix-sharing")
+    step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False),
+                      grouped=grouped)
+    return w, batch, step
 
 
 def run_ours(args):
@@ -279,24 +417,20 @@ def run_ours(args):
         dist.init_process_group("nccl")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    from paged_kv_cache_138_gb300 import accounting
     from paged_kv_cache_138_gb300 import build as nb
     if rank == 0:
         nb.build()
     if world > 1:
         torch.distributed.barrier()
     w, batch, step = setup(args, device, rank)
-    kv_bytes = accounting.step_kv_bytes(batch.context_lens, w.num_kv_heads, w.head_dim,
-                                        layers=w.num_layers)
+    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
+    cfg, kv_bytes, unique_kv = workload_config(w, batch.block_tables, batch.context_lens,
+                                               batch.num_blocks, l2_bytes)
     stream = torch.cuda.current_stream(device)
     # a step whose bytes L2 could hold across steps gets L2 flushed between
     # timed steps (a write of a buffer 4x the L2 size); each step is then timed
     # by its own event pair so the flush stays outside the measured time
-    l2_bytes = torch.cuda.get_device_properties(device).L2_cache_size
-    step_bytes = kv_bytes / w.num_layers
-    if args.workload == "prefix-sharing":
-        step_bytes = accounting.unique_kv_bytes(batch.block_tables, batch.context_lens,
-                                                w.block_size, w.num_kv_heads, w.head_dim)
+    step_bytes = unique_kv if unique_kv is not None else kv_bytes / w.num_layers
     flush_buf = (torch.empty(max(4 * l2_bytes, 512 << 20), dtype=torch.uint8, device=device)
                  if step_bytes < 4 * l2_bytes else None)
 
@@ -321,49 +455,31 @@ def run_ours(args):
         step.apply_cow(stream)
         step.run(stream)
 
+    clocks = ClockSampler(device.index).start()
     for _ in range(max(args.warmup, 3)):
         one_step()
     torch.cuda.synchronize(device)
     step.check_errors()
 
-    # ---- device-resident timed region ----------------------------------------------
-    sampled_steps = (args.steps + ATTN_SAMPLE_EVERY - 1) // ATTN_SAMPLE_EVERY
-    attn_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(sampled_steps * step.num_layers)]
+    # ---- device-resident timed region: exactly --steps steps -------------------------
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.ready()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(device)
-    k_attn = [0]
-    n_timed = [0]
-
-    def timed_step():
-        step.apply_cow(stream)
-        sample = n_timed[0] % ATTN_SAMPLE_EVERY == 0
-        n_timed[0] += 1
-        for i in range(step.num_layers):
-            if not step.fused:
-                step.cache_write(i, stream)
-            if sample:
-                attn_events[k_attn[0]][0].record(stream)
-            step.attend(i, stream)
-            if sample:
-                attn_events[k_attn[0]][1].record(stream)
-                k_attn[0] += 1
-
-    with ClockSampler(device.index) as clocks:
-        if flush_buf is None:
-            start.record(stream)
-            for _ in range(args.steps):
-                timed_step()
-            stop.record(stream)
-            torch.cuda.synchronize(device)
-        else:
-            step_ms = per_step_timed(args.steps, timed_step)
+    t_host0 = time.time()
+    if flush_buf is None:
+        start.record(stream)
+        for _ in range(args.steps):
+            one_step()
+        stop.record(stream)
+        torch.cuda.synchronize(device)
+    else:
+        step_ms = per_step_timed(args.steps, one_step)
+    t_host1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(stop) if flush_buf is None else sum(step_ms)
-    attn_ms = sum(a.elapsed_time(b) for a, b in attn_events[:k_attn[0]]) / k_attn[0]
     step.check_errors()
     if world > 1:
         t = torch.tensor([elapsed_ms], device=device)
@@ -372,37 +488,55 @@ def run_ours(args):
     ms_per_step = elapsed_ms / args.steps
     value = world * kv_bytes / (ms_per_step / 1e3) / 1e9
 
+    # ---- the attention launch alone: ROOFLINE_LAUNCHES back to back between two
+    # events (layer after layer), each launch waiting on nothing but the previous one
+    n_attn = max(ROOFLINE_LAUNCHES, step.num_layers)
+    for i in range(step.num_layers):
+        step.attend(i, stream)
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    t_attn0 = time.time()
+    a0.record(stream)
+    for j in range(n_attn):
+        step.attend(j % step.num_layers, stream)
+    a1.record(stream)
+    torch.cuda.synchronize(device)
+    t_attn1 = time.time()
+    attn_ms = a0.elapsed_time(a1) / n_attn
+    step.check_errors()
+
     # ---- end to end through the public API from pinned host buffers ----------------
-    # every step copies its inputs from pinned host memory and its output back;
-    # the copies of step k+1 and k-1 run on a copy stream beside step k's kernels
-    e2e_steps = args.e2e_steps or max(3, min(args.steps, 500))
+    # every step copies its inputs (q, new K/V, slots, block tables, context
+    # lengths) from pinned host memory and its output back; the copies of step
+    # k+1 and k-1 run on a copy stream beside step k's kernels
+    per_window = args.e2e_steps or E2E_STEPS_PER_WINDOW
     h2d, d2h = step.host_bytes_per_step()
     host = step.host_buffers()
     step.run_from_host_pipelined([host] * 3, [host["out"]] * 3, stream)
     torch.cuda.synchronize(device)
     if world > 1:
         torch.distributed.barrier()
-    # timed as E2E_CHUNKS back-to-back windows, each with its own warm start;
-    # the median window is reported (one host stall -- a page fault, another
-    # process -- would otherwise be spread over every step of a single window)
+    # E2E_WINDOWS back-to-back windows, each with its own warm start; the median
+    # window is reported (one host stall -- a page fault, another process --
+    # would otherwise be spread over every step of a single window)
     import gc
-    chunk = max(1, e2e_steps // E2E_CHUNKS)
     windows = []
     gc.disable()
     try:
-        for _ in range(E2E_CHUNKS):
+        for _ in range(E2E_WINDOWS):
             if flush_buf is not None:
                 # L2 flushed between steps: no overlap of neighbouring steps
-                windows.append(sum(per_step_timed(chunk, lambda: step.run_from_host(stream)))
-                               / chunk)
+                windows.append(sum(per_step_timed(per_window, lambda: step.run_from_host(stream)))
+                               / per_window)
                 continue
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step.run_from_host_pipelined([host] * chunk, [host["out"]] * chunk, stream)
+            step.run_from_host_pipelined([host] * per_window, [host["out"]] * per_window,
+                                         stream)
             stream.wait_stream(step._pipe.copy)
             e1.record(stream)
             torch.cuda.synchronize(device)
-            windows.append(e0.elapsed_time(e1) / chunk)
+            windows.append(e0.elapsed_time(e1) / per_window)
     finally:
         gc.enable()
     e2e_ms = sorted(windows)[len(windows) // 2]
@@ -436,7 +570,7 @@ def run_ours(args):
     flushed = None
     if flush_buf is None and step_bytes < 8 * l2_bytes:
         flush_buf = torch.empty(max(4 * l2_bytes, 512 << 20), dtype=torch.uint8, device=device)
-        n_fl = min(args.steps, 500)
+        n_fl = min(max(args.steps, 50), 500)
         fl_ms = sum(per_step_timed(n_fl, one_step)) / n_fl
         flushed = {"ms_per_step": fl_ms, "value": world * kv_bytes / (fl_ms / 1e3) / 1e9,
                    "unit": "GB/s", "steps": n_fl,
@@ -444,6 +578,7 @@ def run_ours(args):
                            "after each" % (flush_buf.numel() >> 20)}
         flush_buf = None
         step.check_errors()
+    clocks.stop()
 
     if rank != 0:
         if world > 1:
@@ -451,72 +586,50 @@ def run_ours(args):
         return 0
 
     peak, peak_kind = hbm_peak()
-    layer_kv = kv_bytes / w.num_layers
-    unique_kv = None
-    if args.workload == "prefix-sharing":
-        # forked samples share prompt blocks: the roofline counts each distinct
-        # (block, row) once -- what HBM must deliver at minimum
-        unique_kv = accounting.unique_kv_bytes(batch.block_tables, batch.context_lens,
-                                               w.block_size, w.num_kv_heads, w.head_dim)
-        layer_kv = unique_kv
+    # forked samples share prompt blocks: the roofline counts each distinct
+    # (block, row) once -- what HBM must deliver at minimum
+    layer_kv = unique_kv if unique_kv is not None else kv_bytes / w.num_layers
     achieved = layer_kv / (attn_ms / 1e3) / 1e9
     tr = traffic_record(("fused/" if step.fused else "") + "paged_attention_decode/" +
                         args.workload + ("" if w.block_size == 16 else "/bs%d" % w.block_size))
+    share = attn_ms * step.num_layers / ms_per_step
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": tr["dram_bytes_per_launch"] if tr else None,
                 "algorithmic_bytes_per_launch": layer_kv,
-                "timing": "CUDA events around the attention launch on every %dth timed step "
-                          "(%d launches)" % (ATTN_SAMPLE_EVERY, k_attn[0]),
+                "launch_ms": attn_ms, "launches": n_attn,
+                "timing": "CUDA events around %d back-to-back attention launches (layers in "
+                          "turn), independent of --steps; launch_ms = elapsed / launches"
+                          % n_attn,
+                "launches_x_layers_over_step": share,
+                "consistency": ("the launch alone takes %.1f %% of the step per layer: the "
+                                "rest of the step is %s" % (100 * share, "the copy-on-write "
+                                "copy" if batch.cow_pairs.shape[0] else
+                                "stream gaps between launches") if share <= 1.0 else
+                                "the launch alone is slower than its share of the step"),
                 "kernel": ("paged_attention_decode_grouped%s (%sshared-prefix + own-tile "
-                           "units, LSE merge, CUDA events)"
+                           "units, then the LSE merge kernel)"
                            % (("_fused", "cache write + ") if step.fused else ("", ""))
                            if step.groups is not None else
-                           "paged_attention_decode_fused (cache write + split kernel + LSE "
-                           "merge, CUDA events)" if step.fused else
-                           "paged_attention_decode (split kernel + LSE merge, CUDA events)"),
+                           "paged_attention_decode_fused (cache write + split kernel, then "
+                           "the LSE merge kernel)" if step.fused else
+                           "paged_attention_decode (split kernel, then the LSE merge kernel)"),
+                "clocks": clocks.summary(t_attn0, t_attn1),
                 "frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS}
     cpu = None
     if not args.no_cpu_baseline:
-        import numpy as np
-        rng = np.random.default_rng(3)
-        S = batch.num_seqs
-        seqs = sorted(rng.choice(S, size=min(S, 16), replace=False).tolist())
-        tot_t, tot_kv, threads = cpu_oracle_sample(step, 0, seqs, list(range(w.num_q_heads)),
-                                                   min_seconds=10.0)
-        cpu = {"value": tot_kv / tot_t / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": "%d random of %d sequences x all %d heads of layer 0 (reshape_and_cache "
-                         "+ attention), repeated for %.1f s (fp64 C oracle, OpenMP)" % (
-                             len(seqs), S, w.num_q_heads, tot_t)}
-        # the same oracle on one core, on the first two of those sequences
-        t1, kv1, _ = cpu_oracle_sample(step, 0, seqs[:2], list(range(w.num_q_heads)),
-                                       min_seconds=3.0, threads=1)
-        cpu["single_thread"] = {"value": kv1 / t1 / 1e9, "unit": "GB/s", "cores": 1,
-                                "sample": "%d sequences x all %d heads, repeated for %.1f s" % (
-                                    min(2, len(seqs)), w.num_q_heads, t1)}
+        o_tables, o_lens, _, _, _ = oracle_metadata(w)
+        cpu = cpu_baseline(w, o_tables, o_lens)
     launches = step.kernel_launches_per_step() + (1 if batch.cow_pairs.shape[0] else 0)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16 (fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": args.workload, "description": w.description,
-                   "fused_cache_write": step.fused,
-                   "grouped_shared_prefix": step.groups is not None,
-                   "num_seqs": batch.num_seqs, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "block_size": w.block_size, "layers": w.num_layers,
-                   "tokens": int(batch.context_lens.sum()), "kv_bytes_per_step": kv_bytes,
-                   "unique_kv_bytes_per_step": unique_kv,
-                   "pool_blocks": batch.num_blocks,
-                   "tail_waste_pct": 100.0 * float(sum(
-                       -(-int(L) // w.block_size) * w.block_size - int(L)
-                       for L in batch.context_lens)) / float(sum(
-                       -(-int(L) // w.block_size) * w.block_size for L in batch.context_lens)),
-                   "l2": ("inputs larger than L2 (%.0f MB per step vs %.0f MB L2); no flush"
-                          % (step_bytes / 1e6, l2_bytes / 1e6)) if flush_buf is None else
-                         ("L2 flushed between timed steps (%d MiB write, outside the "
-                          "per-step events)" % (flush_buf.numel() >> 20))},
+        "config": cfg,
+        "impl_config": {"fused_cache_write": step.fused,
+                        "grouped_shared_prefix": step.groups is not None,
+                        "split_tokens": step.split_tokens()},
         "seq_steps_per_s": world * batch.num_seqs / (ms_per_step / 1e3),
         "pct_of_hbm_peak": {"measured": 100 * value / world / peak if peak_kind == "measured"
                             else None, "nominal_8tbs": 100 * value / world / NOMINAL_HBM_GBS},
@@ -525,13 +638,17 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "mean_ms_per_step": e2e_mean_ms, "windows": len(windows),
-                "steps_per_window": chunk,
-                "timing": "median of %d windows of %d pipelined steps" % (len(windows), chunk)},
+                "steps_per_window": per_window,
+                "timing": "median of %d windows of %d pipelined steps" % (len(windows),
+                                                                           per_window)},
         "l2_flushed": flushed,
         "graph": {"ms_per_step": graph_ms, "value": world * kv_bytes / (graph_ms / 1e3) / 1e9,
                   "unit": "GB/s", "note": "same step replayed from a CUDA graph"},
         "gpu_launches": launches * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": dict(clocks.summary(t_host0, t_host1),
+                       window_s=round(t_host1 - t_host0, 4),
+                       note="samples stamped inside the timed region"),
+        "clocks_whole_run": clocks.summary(),
     }
     print(json.dumps(line))
     if world > 1:

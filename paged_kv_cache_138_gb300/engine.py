@@ -175,6 +175,12 @@ class DecodeStep:
             return self.num_layers * (2 if self.fused else 3)
         return self.num_layers * ((1 if self.fused else 2) + merge)
 
+    def split_tokens(self):
+        """Tokens per split unit of this batch's attention launches."""
+        w = self.batch.workload
+        return ops.split_tokens(self.batch.num_seqs, w.num_kv_heads, self.batch.max_blocks,
+                                w.block_size)
+
     def check_errors(self):
         """Synchronise and raise if a kernel reported a device error code."""
         code = ops.read_error_word(self.dev_err)
