@@ -46,7 +46,8 @@ extern "C" {
 #define PKV_DEV_BAD_BLOCK_ID 1     /* table entry outside [0, num_blocks) */
 #define PKV_DEV_BAD_CONTEXT_LEN 2  /* context_lens[s] < 0 or > max_blocks * bs */
 #define PKV_DEV_BAD_SLOT 3         /* slot >= num_blocks * block_size */
-#define PKV_DEV_WAIT_TIMEOUT 4     /* a bounded wait on a copy gave up */
+#define PKV_DEV_WAIT_TIMEOUT 4     /* a bounded wait on a copy gave up; every
+                                      output of that launch is then undefined */
 #define PKV_DEV_BAD_POSITION 5     /* position outside its block table */
 #define PKV_DEV_BAD_GROUP 6        /* a shared-prefix group whose members do not
                                       share the stated blocks, or too many rows */
@@ -151,9 +152,14 @@ int pkv_paged_attention_decode_fused(void* out, const void* q, const void* k_new
  *     array holds, i.e. when pkv_paged_attention_workspace_bytes(...) for the
  *     same sizes exceeds 16 MiB (16777216 bytes).
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
- *   - The first call on a device looks up the scratch array's device address
- *     with that device current (cudaGetSymbolAddress); make that first call
- *     before any stream capture.
+ *   - Every call made outside stream capture looks the scratch array's
+ *     device address up again in the current context (cudaGetSymbolAddress,
+ *     which allocates nothing), so a context created anew on the device
+ *     (after cudaDeviceReset, or another driver context made current) uses
+ *     the array's address in that context.  A call on a stream that is being
+ *     captured reuses the address the device's last uncaptured call found:
+ *     make the first call on a device, with that device current, before any
+ *     stream capture.
  *   - Every call shares the one array and leaves its contents behind; nothing
  *     in it needs to start at zero.  Calls whose kernels overlap on the GPU
  *     (other streams, other host threads) race on it: serialise them.

@@ -389,14 +389,22 @@ constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
 // Held by every device that loads this library, until the process exits.
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (host code may not use the symbol itself as a device pointer).
-void* static_scratch_ptr() {
+// Device address of g_static_scratch in the current context.  It is looked up
+// again on every call made outside stream capture (the lookup allocates
+// nothing), so a context created anew on the device -- after
+// cudaDeviceReset, or another driver context made current -- gets the
+// array's address in that context, not a stale one.  A call made while its
+// stream is being captured uses the address the device's last uncaptured
+// call found (the first call on a device must therefore come before any
+// capture).
+void* static_scratch_ptr(cudaStream_t stream) {
   static std::atomic<void*> ptrs[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  void* p = ptrs[dev].load(std::memory_order_acquire);
-  if (p) return p;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return nullptr;
+  if (cap != cudaStreamCaptureStatusNone) return ptrs[dev].load(std::memory_order_acquire);
+  void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return nullptr;
   ptrs[dev].store(p, std::memory_order_release);
   return p;
@@ -420,7 +428,7 @@ extern "C" int pkv_paged_attention_decode_noalloc(void* out, const void* q, cons
   if (need > kStaticScratchBytes) return PKV_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (need > 0) {
-    scratch = static_scratch_ptr();
+    scratch = static_scratch_ptr(static_cast<cudaStream_t>(stream));
     if (!scratch) return PKV_ERR_CUDA;
   }
   return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,

@@ -4,10 +4,12 @@ It serves callers that may not allocate device memory: a plugin inside a host
 framework that owns the whole device memory pool, or a latency-critical path
 that cannot afford an allocation's implicit device synchronisation.  Instead of
 a caller workspace it uses a fixed 16 MiB scratch array inside the library.
-These tests call it through the C ABI and require its output to match the
-workspace entry point's within the attention tolerance, on two calls in a row
-(the second call sees the first call's leftovers in the shared scratch).  This
-file is named to be collected last.
+These tests call it through the C ABI, twice in a row on different shapes (the
+second call sees the first call's leftovers in the shared scratch), and require
+its output to equal the workspace entry point's bit for bit (the same kernels
+run the same split length over the same inputs) and to match the fp64 oracle
+within the attention tolerance.  A call after a warm-up call must leave the
+device's allocated memory unchanged.  This file is named to be collected last.
 """
 import ctypes
 
@@ -15,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import attention as oa
 from parity_helpers import attention_tolerance
 from paged_kv_cache_138_gb300 import workloads as wl
 
@@ -65,8 +68,29 @@ def test_noalloc_matches_workspace_entry_point(native_lib):
         rc = _noalloc(native_lib, out, q, kc, vc, tables, lens, scale, err)
         assert rc == 0
         assert ops.read_error_word(err) == 0
-        diff = (out.double() - ref.double()).abs().max().item()
+        # same kernels, same split length, same inputs: the same bits
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        oracle = oa.paged_attention_decode(q.cpu().numpy(), kc.cpu().numpy(), vc.cpu().numpy(),
+                                           tables.cpu().numpy(), lens.cpu().numpy(), scale)
+        diff = np.abs(out.cpu().numpy().astype(np.float64) - oracle).max()
         assert diff <= attention_tolerance(), diff
+
+
+def test_noalloc_allocates_nothing(native_lib):
+    from paged_kv_cache_138_gb300 import ops
+    q, kc, vc, tables, lens = _case(3, [4096, 2500, 1, 700], 16, 4)
+    out = torch.empty_like(q)
+    err = ops.new_error_word()
+    scale = 1.0 / np.sqrt(D)
+    assert _noalloc(native_lib, out, q, kc, vc, tables, lens, scale, err) == 0   # warm-up
+    torch.cuda.synchronize()
+    torch_before = torch.cuda.memory_allocated()
+    free_before = torch.cuda.mem_get_info()[0]
+    assert _noalloc(native_lib, out, q, kc, vc, tables, lens, scale, err) == 0
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == torch_before
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert ops.read_error_word(err) == 0
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(native_lib):
