@@ -300,6 +300,7 @@ struct TileStream {
   const CUtensorMap* tk;
   const CUtensorMap* tv;
   int warp, lane, g, tile_begin, my_count, issued;
+  bool timed_out;  // a bounded wait of run() gave up (warp-uniform)
   TileIds my_ids;
 
   // ids_limit: tokens at or past it have no block (the context length).
@@ -313,6 +314,7 @@ struct TileStream {
     g = g_;
     tile_begin = tile_begin_;
     my_count = warp < n_here ? (n_here - warp + kWarps - 1) / kWarps : 0;
+    timed_out = false;
     stages = smem + Smem::stages + warp * kStages * kStageBytes;
     bars = reinterpret_cast<uint64_t*>(smem + Smem::bars) + warp * kStages;
     my_ids.a = my_ids.b = -1;
@@ -397,6 +399,7 @@ struct TileStream {
         ++issued;
       }
     }
+    timed_out = !ok;
   }
 };
 
@@ -540,7 +543,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   l += __shfl_xor_sync(kFull, l, 2);
 
   // ---- merge the 4 warps' partial softmax states ------------------------------
-  __syncthreads();  // every issued tile has landed (or timed out); ring is free
+  // every issued tile has landed and the ring is free -- unless a bounded wait
+  // gave up: boxes may then still be in flight into the ring, which the merge
+  // reuses, so the CTA leaves without merging or storing (PKV_DEV_WAIT_TIMEOUT
+  // is reported; the launch's outputs are undefined)
+  if (__syncthreads_or(ts.timed_out)) return;
   float* ml = reinterpret_cast<float*>(smem + Smem::ml);
   float* ob = reinterpret_cast<float*>(smem + Smem::stages);
   if (qrow < G) {
@@ -653,7 +660,8 @@ __device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUt
     l[r] += __shfl_xor_sync(kFull, l[r], 2);
   }
 
-  __syncthreads();
+  // as in split_body: after a wait that gave up, neither merge nor store
+  if (__syncthreads_or(ts.timed_out)) return;
   float* ml = reinterpret_cast<float*>(smem + Smem::ml);
   float* ob = reinterpret_cast<float*>(smem + Smem::stages);
 #pragma unroll

@@ -69,44 +69,71 @@ def test_native_serving_matches_oracle_every_step(native_lib, preemption, groupe
 @pytest.mark.parametrize("grouped", [False, True])
 def test_native_serving_with_device_values_matches_oracle(native_lib, grouped):
     """The configuration the serving benchmark times (values drawn on the
-    device, GQA, shared system prompts): every few steps each decoded row is
-    recomputed by the oracle from the cache as the step left it, the step's
-    q rows and the request's block table."""
+    device, GQA, shared system prompts).  The oracle keeps its own copy of the
+    cache, built from each step's inputs with its own reshape_and_cache
+    (prefill rows, then after copy_blocks the new tokens, at the slots the
+    step names) and copy_blocks; every few steps each decoded row is
+    recomputed from that copy, the step's q rows and block tables.  At the end
+    the device cache must equal the oracle's copy bit for bit."""
     import torch
+    from oracle import cache_ops as oc
     from paged_kv_cache_138_gb300.serving import DeviceRandomValues, NativeServingDriver
+
+    class Recorded(DeviceRandomValues):
+        """Device draws, kept so the host can read them back after the step."""
+        def prefill(self, drv, rids, positions, stream=None):
+            k, v = super().prefill(drv, rids, positions, stream)
+            self.prefill_kv = (k, v)
+            return k, v
+
     hq, hkv = 8, 2
     reqs = wl.serving_requests(SEED + 1, num_requests=24, num_system_prompts=2,
                                system_prompt_len=48, suffix_max=12, new_min=3, new_max=40)
     nb, mb = 64, 8
-    drv = NativeServingDriver(nb, hq, hkv, max_batch=8, max_blocks_per_seq=mb,
-                              values=DeviceRandomValues(3, hq, hkv, device="cuda"),
+    values = Recorded(3, hq, hkv, device="cuda")
+    drv = NativeServingDriver(nb, hq, hkv, max_batch=8, max_blocks_per_seq=mb, values=values,
                               free_order=np.random.default_rng(4).permutation(nb), seed=SEED,
                               grouped=grouped)
     for r in reqs:
         drv.add_request(r.rid, r.prompt, r.max_new_tokens)
+    kc = np.zeros(tuple(drv.k_cache.shape), np.float16)    # the driver's cache starts at 0
+    vc = np.zeros_like(kc)
     worst, rows, steps, shared = 0.0, 0, 0, 0
     while not drv.idle:
+        values.prefill_kv = None
         res = drv.step()
+        a = drv.sets[(drv.steps - 1) % 2]["a"]            # this step's arrays
+        o = drv.sets[(drv.steps - 1) % 2]["out"]
         steps += 1
         assert steps < 500
+        assert o.num_swap_in == 0 and o.num_swap_out == 0
         shared += res["shared_tokens"]
-        B = len(res["rids"])
-        if B == 0 or steps % 3:
-            continue
         torch.cuda.synchronize()
+        if o.num_prefill:
+            k, v = values.prefill_kv
+            oc.reshape_and_cache(k.cpu().numpy(), v.cpu().numpy(),
+                                 a["prefill_slots"][:o.num_prefill], kc, vc)
+        if o.num_cow:
+            oc.copy_blocks([kc], [vc], a["cow_pairs"][:o.num_cow])
+        B = len(res["rids"])
+        if B == 0:
+            continue
+        oc.reshape_and_cache(drv.k_new[:B].cpu().numpy(), drv.v_new[:B].cpu().numpy(),
+                             a["slots"][:B], kc, vc)
+        if steps % 3:
+            continue
         out = res["out"].cpu().numpy().astype(np.float64)
         q = drv.q[:B].cpu().numpy()
-        kc, vc = drv.k_cache.cpu().numpy(), drv.v_cache.cpu().numpy()
-        tables = np.full((B, mb), -1, np.int32)
-        for i, rid in enumerate(res["rids"].tolist()):
-            t = drv.bm.block_table(rid)
-            tables[i, :len(t)] = t
+        tables = np.ascontiguousarray(a["block_tables"][:B])
         lens = (res["positions"] + 1).astype(np.int32)
+        assert (lens == a["context_lens"][:B]).all()
         ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
         worst = max(worst, float(np.abs(out - ref).max()))
         rows += B
     drv.check_errors()
     assert rows > 0 and worst <= attention_tolerance(), worst
+    assert np.array_equal(drv.k_cache.cpu().numpy().view(np.uint16), kc.view(np.uint16))
+    assert np.array_equal(drv.v_cache.cpu().numpy().view(np.uint16), vc.view(np.uint16))
     if grouped:
         assert shared > 0
     drv.bm.check_invariants()
