@@ -78,6 +78,8 @@ def parse(argv=None):
                     help="shared-prefix grouped attention (auto: on for prefix-sharing)")
     ap.add_argument("--block-size", type=int, default=16,
                     help="tokens per KV block: 8, 16, 32 or 64")
+    ap.add_argument("--cow-kernel", action="store_true",
+                    help="copy-on-write copies by copy_blocks, not inside the fused launches")
     return ap.parse_args(argv)
 
 
@@ -403,7 +405,7 @@ def setup(args, device, rank=0):
     grouped = {"on": True, "off": False}.get(getattr(args, "grouped", "auto"),
                                               args.workload == "prefix-sharing")
     step = DecodeStep(batch, device=device, fused=not getattr(args, "unfused", False),
-                      grouped=grouped)
+                      grouped=grouped, fold_cow=not getattr(args, "cow_kernel", False))
     return w, batch, step
 
 
@@ -604,7 +606,7 @@ def run_ours(args):
                 "launches_x_layers_over_step": share,
                 "consistency": ("the launch alone takes %.1f %% of the step per layer: the "
                                 "rest of the step is %s" % (100 * share, "the copy-on-write "
-                                "copy" if batch.cow_pairs.shape[0] else
+                                "copy" if step.cow_launches_per_step() else
                                 "stream gaps between launches") if share <= 1.0 else
                                 "the launch alone is slower than its share of the step"),
                 "kernel": ("paged_attention_decode_grouped%s (%sshared-prefix + own-tile "
@@ -620,7 +622,7 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         o_tables, o_lens, _, _, _ = oracle_metadata(w)
         cpu = cpu_baseline(w, o_tables, o_lens)
-    launches = step.kernel_launches_per_step() + (1 if batch.cow_pairs.shape[0] else 0)
+    launches = step.kernel_launches_per_step() + step.cow_launches_per_step()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -629,6 +631,9 @@ def run_ours(args):
         "config": cfg,
         "impl_config": {"fused_cache_write": step.fused,
                         "grouped_shared_prefix": step.groups is not None,
+                        "cow_copies": ("inside the attention launches" if step.cow is not None
+                                       else "copy_blocks" if batch.cow_pairs.shape[0]
+                                       else None),
                         "split_tokens": step.split_tokens()},
         "seq_steps_per_s": world * batch.num_seqs / (ms_per_step / 1e3),
         "pct_of_hbm_peak": {"measured": 100 * value / world / peak if peak_kind == "measured"

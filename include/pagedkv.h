@@ -230,6 +230,58 @@ int pkv_paged_attention_decode_grouped_fused(
     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
     float scale, void* workspace, size_t workspace_bytes, int32_t* dev_err, void* stream);
 
+/*
+ * Copy-on-write folded into the fused launch: what pkv_copy_blocks of the
+ * step's copy-on-write pairs followed by pkv_paged_attention_decode_fused
+ * (or _grouped_fused) does, in the one attention launch.  "ans20xx day 31"
+ * (fork and copy-on-write): before a forked sequence writes into a block it
+ * shares, the block is copied into a private one and the write goes there.
+ * For each sequence s with cow_block[s] >= 0, logical block cow_block[s] of
+ * its table (the private copy, dst) receives a whole-block copy, K and V of
+ * every KV head of this layer, of physical block cow_src[s] (the shared
+ * source); then the new token is written (into the copy when it falls in
+ * that block) and attention reads the copied block's values.  The unit that
+ * streams the block reads it from cow_src[s] (the bytes the copy will hold)
+ * and stores the staged tile as the copy, so nothing waits for a separate
+ * copy kernel.
+ *   cow_block  int32 [num_seqs] (device): logical block index, -1 for none;
+ *              one per sequence per call (pkv_cow_targets builds it)
+ *   cow_src    int32 [num_seqs] (device): the source physical block
+ * The block must hold some of the sequence's own tokens (below
+ * context_lens[s], past a group's shared prefix), else PKV_DEV_BAD_POSITION;
+ * a source or table entry outside [0, num_blocks) gives PKV_DEV_BAD_BLOCK_ID;
+ * either way no copy is made for s.  block_size must be 8 or 16
+ * (PKV_ERR_UNSUPPORTED otherwise: larger blocks span several tiles).  Other
+ * arguments, layouts and errors as pkv_paged_attention_decode_fused /
+ * pkv_paged_attention_decode_grouped_fused.
+ */
+int pkv_paged_attention_decode_fused_cow(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* cow_block,
+    const int32_t* cow_src, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream);
+int pkv_paged_attention_decode_grouped_fused_cow(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+    void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const int32_t* group_first, const int32_t* seq_group, const int32_t* group_shared,
+    int num_groups, int max_shared_tokens, int max_own_tokens, const int32_t* cow_block,
+    const int32_t* cow_src, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * Host helper for the _cow launches (host memory only): for copy-on-write
+ * pairs (src, dst) as pkv_bm_take_cow_pairs returns them, find the sequence
+ * and logical block whose table entry is dst.  cow_block[s] = that logical
+ * block and cow_src[s] = src; -1 / -1 for sequences no pair names.  Returns
+ * PKV_OK; PKV_ERR_BAD_INDEX if a dst appears in no table, or in two places;
+ * PKV_ERR_UNSUPPORTED if one sequence needs two copies (use pkv_copy_blocks).
+ *   pairs int64 [num_pairs, 2], tables int32 [num_seqs, max_blocks] (host)
+ */
+int pkv_cow_targets(const int64_t* pairs, int num_pairs, const int32_t* tables, int num_seqs,
+                    int max_blocks, int32_t* cow_block, int32_t* cow_src);
+
 /* Workspace bytes pkv_paged_attention_decode_grouped needs (host only). */
 size_t pkv_paged_attention_grouped_workspace_bytes(int num_seqs, int num_q_heads,
                                                    int max_blocks_per_seq, int block_size,

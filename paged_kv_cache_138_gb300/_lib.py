@@ -39,6 +39,12 @@ SIGNATURES = {
                                                       _I, _I, _I, _I, _I, _I, _I, _I, _I64, _I,
                                                       _F, _P, _SZ, _P, _P]),
     "pkv_plan_shared_prefix_groups": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "pkv_paged_attention_decode_fused_cow": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I,
+                                                  _I, _I, _I, _I64, _I, _F, _P, _SZ, _P, _P]),
+    "pkv_paged_attention_decode_grouped_fused_cow": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                          _P, _I, _I, _I, _P, _P, _I, _I, _I, _I,
+                                                          _I, _I64, _I, _F, _P, _SZ, _P, _P]),
+    "pkv_cow_targets": (_I, [_P, _I, _P, _I, _I, _P, _P]),
     "pkv_paged_attention_decode_fused": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                               _I64, _I, _F, _P, _SZ, _P, _P]),
     "pkv_paged_attention_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I64,

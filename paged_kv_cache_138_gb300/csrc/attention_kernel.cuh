@@ -86,6 +86,11 @@ struct Params {
   const int32_t* seq_group;     // [S] group of each sequence
   const int32_t* group_first;   // [num_groups + 1] first sequence of each group
   const int32_t* group_shared;  // [num_groups] tokens the whole group shares
+  // copy-on-write folded into a fused launch (nullptr otherwise): sequence s
+  // gets logical block cow_block[s] (-1: none) as a copy of physical block
+  // cow_src[s] before its new token is written there
+  const int32_t* cow_block;     // [S]
+  const int32_t* cow_src;       // [S]
   int64_t num_blocks;
   int num_seqs, num_q_heads, num_kv_heads, max_blocks, max_splits, block_size, num_groups;
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
@@ -304,9 +309,12 @@ struct TileStream {
   TileIds my_ids;
 
   // ids_limit: tokens at or past it have no block (the context length).
+  // Logical block cow_blk (-1: none) is read from physical block cow_from
+  // instead of the table's entry (copy-on-write folded into the launch).
   __device__ __forceinline__ void init(uint8_t* smem, const CUtensorMap* tk_, const CUtensorMap* tv_,
                                        int g_, const int32_t* trow, int tile_begin_, int n_here,
-                                       int ids_limit, const Params& p) {
+                                       int ids_limit, const Params& p, int cow_blk = -1,
+                                       int32_t cow_from = -1) {
     warp = threadIdx.x >> 5;
     lane = threadIdx.x & 31;
     tk = tk_;
@@ -324,7 +332,9 @@ struct TileStream {
       for (int q = 0; q < kBlocksPerTile; ++q) {
         const int tok = first_tok + q * BS;
         int32_t b = -1;
-        if (tok < ids_limit) {
+        if (tok < ids_limit && tok / BS == cow_blk) {
+          b = cow_from;  // checked by the caller
+        } else if (tok < ids_limit) {
           b = __ldg(trow + tok / BS);
           if (b < 0 || b >= p.num_blocks) {
             report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
@@ -436,6 +446,28 @@ __device__ __forceinline__ void store_partial(const Params& p, int64_t row, int 
   }
 }
 
+// Copy-on-write from the staged tile: rows first_row .. first_row + rows - 1
+// of the stage (K and V of KV head g, the whole source block: rows = BS <=
+// 16) are stored as block `dst`, one 16-byte chunk per lane and step; the
+// half-warps write 256 contiguous bytes each.
+template <int BS>
+__device__ __forceinline__ void store_staged_block(uint32_t st, const Params& p, int g,
+                                                   int32_t dst, int first_row, int lane) {
+  static_assert(BS <= kTile, "a copied block must fit in one tile");
+  for (int i = lane; i < BS * 32; i += 32) {
+    const int r = i >> 5, c = i & 15;
+    const bool is_v = (i >> 4) & 1;
+    uint4 val;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                 : "r"(tile_chunk(st, is_v ? 2 : 0, first_row + r, c)));
+    const int64_t at =
+        ((static_cast<int64_t>(dst) * BS + r) * p.num_kv_heads + g) * kHeadDim + c * 8;
+    *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) + at) = val;
+  }
+  __syncwarp();  // every lane has read the stage before it changes again
+}
+
 // One CTA per (KV head, sequence, split of its own tiles).  In grouped launches
 // a sequence's own tiles start after the prefix its group shares, and its
 // partials go after the group's shared splits.
@@ -482,9 +514,37 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   if (tile_begin >= ntiles) return;
   const int n_here = min(p.partition_tiles, ntiles - tile_begin);
 
+  // copy-on-write folded into the launch (FUSED, BS <= 16): the block must
+  // hold some of the sequence's own tokens; the unit whose tile holds it reads
+  // the source block instead and stores the staged rows as the block
+  int cow_blk = -1, cow_tile = -1;
+  int32_t cow_from = -1, cow_to = -1;
+  if constexpr (FUSED && BS <= kTile) {
+    if (p.cow_block) {
+      const int cb = __ldg(p.cow_block + s);
+      if (cb >= 0) {
+        const bool may_report = threadIdx.x == 0 && g == 0 && split == 0;
+        const int32_t from = __ldg(p.cow_src + s);
+        if (cb >= p.max_blocks || cb * BS >= L || cb * BS < own_begin * kTile) {
+          if (may_report) report(p.dev_err, PKV_DEV_BAD_POSITION);
+        } else {
+          const int32_t to = __ldg(p.block_tables + static_cast<int64_t>(s) * p.max_blocks + cb);
+          if (from < 0 || from >= p.num_blocks || to < 0 || to >= p.num_blocks) {
+            if (may_report) report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
+          } else {
+            cow_blk = cb;
+            cow_tile = cb * BS / kTile;
+            cow_from = from;
+            cow_to = to;
+          }
+        }
+      }
+    }
+  }
+
   TileStream<BS> ts;
   ts.init(smem, &tmap_k, &tmap_v, g, p.block_tables + static_cast<int64_t>(s) * p.max_blocks,
-          tile_begin, n_here, L, p);
+          tile_begin, n_here, L, p, cow_blk, cow_from);
 
   // q of this lane's row as m16n8k16 A fragments (raw fp16; scale applied to S)
   uint32_t qa[8][2];
@@ -520,8 +580,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   for (int nd = 0; nd < 16; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
   ts.run(p.dev_err, [&](uint32_t st, int tile, TileIds t) {
     if (FUSED && tile == new_tile) {
-      // cache write of the new token: global slot and the staged row
-      const int32_t blk = (BS < kTile && new_row >= BS) ? t.b : t.a;
+      // cache write of the new token: global slot and the staged row (a
+      // block being copied is written at its copy, not at its source)
+      int32_t blk = (BS < kTile && new_row >= BS) ? t.b : t.a;
+      if (tile == cow_tile && (L - 1) / BS == cow_blk) blk = cow_to;
       const int row_in_block = (L - 1) % BS;
       const int c = lane & 15;
       const bool is_v = lane >= 16;
@@ -536,6 +598,12 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
                    : "memory");
       fence_proxy_async_smem();
       __syncwarp();
+    }
+    if constexpr (FUSED && BS <= kTile) {
+      // the copied block, new token included, before process_tile zeroes the
+      // V rows past the context in the stage
+      if (tile == cow_tile)
+        store_staged_block<BS>(st, p, g, cow_to, (cow_blk * BS) % kTile, lane);
     }
     process_tile(st, qa, min(kTile, L - tile * kTile), lane, p.scale_log2, m, l, o);
   });

@@ -507,3 +507,46 @@ extern "C" int pkv_plan_shared_prefix_groups(const int32_t* tables, const int32_
   *max_own_tokens = max_own;
   return PKV_OK;
 }
+
+// ---- copy-on-write targets for the folded copy (host) ------------------------------
+// Each pair's dst is a private block (reference count 1 after the copy), so it
+// names exactly one (sequence, logical block); the fused _cow launches take
+// one such block per sequence.
+extern "C" int pkv_cow_targets(const int64_t* pairs, int num_pairs, const int32_t* tables,
+                               int num_seqs, int max_blocks, int32_t* cow_block,
+                               int32_t* cow_src) {
+  if (num_pairs < 0 || num_seqs < 0 || max_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!tables || !cow_block || !cow_src)) return PKV_ERR_INVALID_ARG;
+  if (num_pairs > 0 && !pairs) return PKV_ERR_INVALID_ARG;
+  for (int s = 0; s < num_seqs; ++s) cow_block[s] = cow_src[s] = -1;
+  struct Target {
+    int64_t src;
+    int hits;
+  };
+  std::unordered_map<int64_t, Target> by_dst;
+  by_dst.reserve(static_cast<size_t>(num_pairs) * 2);
+  for (int i = 0; i < num_pairs; ++i) {
+    const int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+    if (src < 0 || src > INT32_MAX || dst < 0 || dst > INT32_MAX) return PKV_ERR_BAD_INDEX;
+    if (!by_dst.emplace(dst, Target{src, 0}).second) return PKV_ERR_BAD_INDEX;
+  }
+  bool two_in_one = false;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int32_t* row = tables + static_cast<int64_t>(s) * max_blocks;
+    for (int j = 0; j < max_blocks; ++j) {
+      if (row[j] < 0) continue;
+      const auto it = by_dst.find(row[j]);
+      if (it == by_dst.end()) continue;
+      ++it->second.hits;
+      if (cow_block[s] >= 0) {
+        two_in_one = true;
+        continue;
+      }
+      cow_block[s] = j;
+      cow_src[s] = static_cast<int32_t>(it->second.src);
+    }
+  }
+  for (const auto& kv : by_dst)
+    if (kv.second.hits != 1) return PKV_ERR_BAD_INDEX;  // in no table, or in two places
+  return two_in_one ? PKV_ERR_UNSUPPORTED : PKV_OK;
+}

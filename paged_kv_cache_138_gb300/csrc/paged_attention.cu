@@ -135,7 +135,8 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
            int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
            size_t workspace_bytes, int32_t* dev_err, void* stream, bool fused,
-           const Groups& groups = Groups()) {
+           const Groups& groups = Groups(), const int32_t* cow_block = nullptr,
+           const int32_t* cow_src = nullptr) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -147,6 +148,10 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PKV_ERR_INVALID_ARG;
   if (fused && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+  if ((cow_block != nullptr) != (cow_src != nullptr) || (cow_block && !fused))
+    return PKV_ERR_INVALID_ARG;
+  // a copied block is staged whole by one tile only for block sizes <= 16
+  if (cow_block && block_size > kTile) return PKV_ERR_UNSUPPORTED;
   const uintptr_t align = reinterpret_cast<uintptr_t>(k_cache) |
                           reinterpret_cast<uintptr_t>(v_cache) |
                           reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new);
@@ -202,6 +207,8 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   p.seq_group = grouped ? groups.seq_group : nullptr;
   p.group_first = groups.first;
   p.group_shared = groups.shared;
+  p.cow_block = cow_block;
+  p.cow_src = cow_src;
   p.num_groups = groups.num_groups;
   p.own_tiles_cap = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition *
                     partition;
@@ -373,6 +380,41 @@ extern "C" int pkv_paged_attention_decode_fused(void* out, const void* q, const 
                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                            max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
                            true);
+}
+
+extern "C" int pkv_paged_attention_decode_fused_cow(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, const int32_t* context_lens, const int32_t* cow_block,
+    const int32_t* cow_src, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!cow_block || !cow_src) return PKV_ERR_INVALID_ARG;
+  return pkv::attn::decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                           num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                           max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
+                           true, pkv::attn::Groups(), cow_block, cow_src);
+}
+
+extern "C" int pkv_paged_attention_decode_grouped_fused_cow(
+    void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+    void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const int32_t* group_first, const int32_t* seq_group, const int32_t* group_shared,
+    int num_groups, int max_shared_tokens, int max_own_tokens, const int32_t* cow_block,
+    const int32_t* cow_src, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int64_t num_blocks, int max_blocks_per_seq, float scale, void* workspace,
+    size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  pkv::attn::Groups gr;
+  gr.first = group_first;
+  gr.seq_group = seq_group;
+  gr.shared = group_shared;
+  gr.num_groups = num_groups;
+  gr.max_shared_tokens = max_shared_tokens;
+  gr.max_own_tokens = max_own_tokens;
+  if (!group_first || !cow_block || !cow_src) return PKV_ERR_INVALID_ARG;
+  return pkv::attn::decode(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                           num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                           max_blocks_per_seq, scale, workspace, workspace_bytes, dev_err, stream,
+                           true, gr, cow_block, cow_src);
 }
 
 // ---- allocation-free variant ------------------------------------------------------

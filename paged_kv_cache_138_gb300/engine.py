@@ -13,6 +13,7 @@ import torch
 
 from . import ops
 from . import workloads as wl
+from ._lib import PKV_ERR_UNSUPPORTED, PagedKVError
 from .scenario import DecodeBatch
 
 
@@ -23,14 +24,16 @@ class DecodeStep:
     buffers (sequential or pipelined)."""
 
     def __init__(self, batch: DecodeBatch, device=None, num_layers=None, host_values=None,
-                 fused=False, grouped=False):
+                 fused=False, grouped=False, fold_cow=True):
         """host_values: None draws q/K/V on the device (torch generator seeded by
         the workload); otherwise the tuple of ``workloads.host_tensors`` (numpy).
         fused: each layer is one launch of the fused cache-write + attention
         kernel instead of reshape_and_cache followed by attention.
         grouped: sequences sharing leading blocks (forked samples) are planned
         into groups whose shared prefix is streamed once (with fused: one
-        launch writing the new tokens and attending)."""
+        launch writing the new tokens and attending).
+        fold_cow: with fused, the batch's copy-on-write copies are made inside
+        each layer's attention launch instead of by copy_blocks."""
         self.fused = bool(fused)
         w = batch.workload
         self.batch = batch
@@ -59,6 +62,17 @@ class DecodeStep:
         self.context_lens = torch.from_numpy(batch.context_lens).to(dev)
         self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(dev)
         self.cow_pairs = torch.from_numpy(batch.cow_pairs).to(dev)
+        # fused steps make the copy-on-write copies inside each layer's
+        # attention launch (one copy per sequence, block size <= 16); others,
+        # or a sequence needing two copies in one step, use copy_blocks
+        self.cow = None
+        if self.fused and batch.cow_pairs.shape[0] and bs <= 16 and fold_cow:
+            try:
+                cb, cs = ops.cow_targets(batch.cow_pairs, batch.block_tables)
+                self.cow = (torch.from_numpy(cb).to(dev), torch.from_numpy(cs).to(dev))
+            except PagedKVError as e:
+                if e.status != PKV_ERR_UNSUPPORTED:
+                    raise
         self.out = torch.empty((L, S, Hq, D), dtype=torch.float16, device=dev)
         self.groups = None
         if grouped:
@@ -78,8 +92,9 @@ class DecodeStep:
 
     # ---- device-resident step ---------------------------------------------------
     def apply_cow(self, stream=None):
-        """copy_blocks for the batch's copy-on-write pairs, every layer."""
-        if self.cow_pairs.shape[0] == 0:
+        """copy_blocks for the batch's copy-on-write pairs, every layer (nothing
+        when the attention launches make the copies)."""
+        if self.cow_pairs.shape[0] == 0 or self.cow is not None:
             return
         ops.copy_blocks([self.k_cache[i] for i in range(self.num_layers)],
                         [self.v_cache[i] for i in range(self.num_layers)],
@@ -119,7 +134,7 @@ class DecodeStep:
                         b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i],
                         self.v_cache[i], b.block_tables, b.context_lens, gf, sg, gs, mx, mo,
                         self.scale, workspace=self.workspace, dev_err=self.dev_err,
-                        stream=stream, prepare=True)
+                        stream=stream, prepare=True, cow=self.cow)
                 return ops.paged_attention_decode_grouped(
                     b.out[i], b.q[i], self.k_cache[i], self.v_cache[i], b.block_tables,
                     b.context_lens, gf, sg, gs, mx, mo, self.scale, workspace=self.workspace,
@@ -128,7 +143,7 @@ class DecodeStep:
                 return ops.paged_attention_decode_fused(
                     b.out[i], b.q[i], b.k_new[i], b.v_new[i], self.k_cache[i], self.v_cache[i],
                     b.block_tables, b.context_lens, self.scale, workspace=self.workspace,
-                    dev_err=self.dev_err, stream=stream, prepare=True)
+                    dev_err=self.dev_err, stream=stream, prepare=True, cow=self.cow)
             return ops.paged_attention_decode(
                 b.out[i], b.q[i], self.k_cache[i], self.v_cache[i], b.block_tables,
                 b.context_lens, self.scale, workspace=self.workspace, dev_err=self.dev_err,
@@ -165,6 +180,10 @@ class DecodeStep:
         """Launch the captured step (capture_graph) with one call."""
         self.graph.replay()
         return self.out
+
+    def cow_launches_per_step(self):
+        """copy_blocks launches of one step (apply_cow): 0 when folded."""
+        return 1 if self.cow_pairs.shape[0] and self.cow is None else 0
 
     def kernel_launches_per_step(self):
         """Kernels of this library one run() launches (COW copies excluded)."""

@@ -146,9 +146,11 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens,
 
 def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_tables,
                                  context_lens, scale, workspace=None, dev_err=None, stream=None,
-                                 prepare=False):
+                                 prepare=False, cow=None):
     """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
     sequence (slot from its block table) and attend over context_lens[s] tokens.
+    cow=(cow_block, cow_src) (int32 [S] device tensors, see cow_targets) also
+    makes each sequence's copy-on-write copy in the same launch.
     prepare=True returns a PreparedLaunch instead of launching."""
     _dev(q, "q", torch.float16, 3)
     _dev(out, "out", torch.float16, 3)
@@ -169,6 +171,16 @@ def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_t
     if need and workspace is None:
         workspace = alloc_workspace(S, Hq, max_blocks, q.device, bs)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if cow is not None:
+        cb, cs = _cow_args(cow, S)
+        args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                _ptr(block_tables), _ptr(context_lens), _ptr(cb), _ptr(cs), S, Hq, Hkv, D, bs,
+                nb, max_blocks, float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err),
+                _stream_handle(stream))
+        keep = (out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, cb, cs,
+                workspace, dev_err, stream)
+        return _issue(lib().pkv_paged_attention_decode_fused_cow, args,
+                      "paged_attention_decode_fused_cow", keep, prepare, out)
     args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
             _ptr(block_tables), _ptr(context_lens), S, Hq, Hkv, D, bs, nb, max_blocks,
             float(scale), _ptr(workspace), ws_bytes, _ptr(dev_err), _stream_handle(stream))
@@ -176,6 +188,33 @@ def paged_attention_decode_fused(out, q, k_new, v_new, k_cache, v_cache, block_t
             dev_err, stream)
     return _issue(lib().pkv_paged_attention_decode_fused, args, "paged_attention_decode_fused",
                   keep, prepare, out)
+
+
+def _cow_args(cow, S):
+    cb, cs = cow
+    _dev(cb, "cow_block", torch.int32, 1)
+    _dev(cs, "cow_src", torch.int32, 1)
+    if cb.shape[0] != S or cs.shape[0] != S:
+        raise ValueError("cow_block / cow_src must be int32 [num_seqs]")
+    return cb, cs
+
+
+def cow_targets(pairs, block_tables):
+    """Host (native): copy-on-write pairs (src, dst) -> (cow_block, cow_src),
+    int32 [S] numpy arrays for the fused launches' ``cow`` argument: the logical
+    block of each sequence whose table holds a pair's dst, and that pair's src
+    (-1 where none).  Raises PagedKVError (UNSUPPORTED) if a sequence needs
+    two copies in one step."""
+    import numpy as np
+    pr = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    S = tables.shape[0]
+    cb = np.empty(max(S, 1), np.int32)
+    cs = np.empty(max(S, 1), np.int32)
+    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    rc = lib().pkv_cow_targets(p(pr), pr.shape[0], p(tables), S, tables.shape[1], p(cb), p(cs))
+    check(rc, "cow_targets")
+    return cb[:S], cs[:S]
 
 
 def reshape_and_cache(k, v, slot_mapping, k_cache, v_cache, dev_err=None, stream=None,
@@ -343,10 +382,11 @@ def paged_attention_decode_grouped_fused(out, q, k_new, v_new, k_cache, v_cache,
                                          context_lens, group_first, seq_group, group_shared,
                                          max_shared_tokens, max_own_tokens, scale,
                                          workspace=None, dev_err=None, stream=None,
-                                         prepare=False):
+                                         prepare=False, cow=None):
     """One launch: store k_new[s]/v_new[s] at position context_lens[s] - 1 of each
     sequence (a block past its group's shared prefix) and attend as
-    paged_attention_decode_grouped."""
+    paged_attention_decode_grouped.  cow=(cow_block, cow_src) also makes the
+    copy-on-write copies in the same launch (see paged_attention_decode_fused)."""
     _dev(q, "q", torch.float16, 3)
     _dev(out, "out", torch.float16, 3)
     _dev(k_new, "k_new", torch.float16, 3)
@@ -370,6 +410,17 @@ def paged_attention_decode_grouped_fused(out, q, k_new, v_new, k_cache, v_cache,
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if cow is not None:
+        cb, cs = _cow_args(cow, S)
+        args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                _ptr(block_tables), _ptr(context_lens), _ptr(group_first), _ptr(seq_group),
+                _ptr(group_shared), G, int(max_shared_tokens), int(max_own_tokens), _ptr(cb),
+                _ptr(cs), S, Hq, Hkv, D, bs, nb, max_blocks, float(scale), _ptr(workspace),
+                ws_bytes, _ptr(dev_err), _stream_handle(stream))
+        keep = (out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, group_first,
+                seq_group, group_shared, cb, cs, workspace, dev_err, stream)
+        return _issue(lib().pkv_paged_attention_decode_grouped_fused_cow, args,
+                      "paged_attention_decode_grouped_fused_cow", keep, prepare, out)
     args = (_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
             _ptr(block_tables), _ptr(context_lens), _ptr(group_first), _ptr(seq_group),
             _ptr(group_shared), G, int(max_shared_tokens), int(max_own_tokens), S, Hq, Hkv, D,

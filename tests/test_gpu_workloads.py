@@ -1,6 +1,7 @@
-"""Every benchmark workload at its full size, run exactly as bench.py runs it
-(DecodeStep: copy_blocks for COW pairs, then per layer reshape_and_cache and
-paged attention), checked against the oracle.
+"""Every benchmark workload at its full size, run through DecodeStep as
+bench.py runs it (copy_blocks for COW pairs, then per layer reshape_and_cache
+and paged attention; the prefix-sharing step also in the benchmark's fused,
+grouped form with the copies inside the launch), checked against the oracle.
 
 The oracle gets host copies of the caches taken BEFORE the step and applies its
 own copy_blocks and reshape_and_cache; nothing the GPU wrote is an oracle input.
@@ -23,14 +24,15 @@ pytestmark = pytest.mark.gpu
 TOL = attention_tolerance()
 
 
-def run_and_check(name, layers_checked, rows_per_layer, all_rows=False):
+def run_and_check(name, layers_checked, rows_per_layer, all_rows=False, fused=False,
+                  grouped=False, whole_cache=False):
     from paged_kv_cache_138_gb300.engine import DecodeStep
     from paged_kv_cache_138_gb300.scenario import prepare_batch
     w = wl.WORKLOADS[name]
     batch = prepare_batch(w)
     tables, lens, slots, pairs, nb = oracle_batch(w)
     assert np.array_equal(batch.block_tables, tables) and np.array_equal(batch.slot_mapping, slots)
-    step = DecodeStep(batch)
+    step = DecodeStep(batch, fused=fused, grouped=grouped)
     before = {i: (step.k_cache[i].cpu().numpy(), step.v_cache[i].cpu().numpy())
               for i in layers_checked}
     step.apply_cow()
@@ -58,6 +60,12 @@ def run_and_check(name, layers_checked, rows_per_layer, all_rows=False):
             err = np.abs(gpu[si, hi] - ref)
         assert np.isfinite(gpu).all()
         worst = max(worst, float(err.max()))
+        if whole_cache:
+            # every block: copies, new tokens and untouched blocks, bit for bit
+            assert np.array_equal(step.k_cache[i].cpu().numpy().view(np.uint16),
+                                  kc.view(np.uint16))
+            assert np.array_equal(step.v_cache[i].cpu().numpy().view(np.uint16),
+                                  vc.view(np.uint16))
         # the new token's K/V landed at its slot, bit for bit
         bs = w.block_size
         for s in rng.integers(0, S, size=8):
@@ -84,6 +92,14 @@ def test_gqa_32_8_full_size(native_lib):
 
 def test_prefix_sharing_full_size(native_lib):
     run_and_check("prefix-sharing", [0], 0, all_rows=True)
+
+
+def test_prefix_sharing_full_size_as_benchmarked(native_lib):
+    """The benchmark's form of the step: one fused grouped launch that also
+    makes the 120 copy-on-write copies; the whole cache must equal the
+    oracle's copy_blocks + reshape_and_cache, every output row the oracle's."""
+    run_and_check("prefix-sharing", [0], 0, all_rows=True, fused=True, grouped=True,
+                  whole_cache=True)
 
 
 def test_llama2_7b_32_layer_full_size(native_lib):
