@@ -28,7 +28,9 @@
 //    with ldmatrix from the swizzled tiles (query heads are the MMA rows).
 //  * Online softmax in base 2 per query row with a lazy rescale: the running
 //    max only moves when a tile max exceeds it by more than 8, so most tiles
-//    skip rescaling and every weight stays <= 2^8 (exact in fp16 range).
+//    skip rescaling and every weight stays <= 2^8 (exact in fp16 range).  The
+//    weights are rounded to fp16 once, for the P.V product, and the running
+//    sum adds those same fp16 values.
 //  * The 4 warps' (m, l, o) are merged in shared memory.  Sequences that need
 //    one split write fp16 output directly; longer ones write fp32 partials that
 //    a second small kernel merges by log-sum-exp.
@@ -200,8 +202,10 @@ __device__ __forceinline__ void process_tile(uint32_t st, const uint32_t (&qa)[8
   }
   const float p0 = exp2_approx(x0 - m), p1 = exp2_approx(x1 - m);
   const float p2 = exp2_approx(x2 - m), p3 = exp2_approx(x3 - m);
-  l += (p0 + p1) + (p2 + p3);
   const uint32_t pa0 = pack_half2(p0, p1), pa2 = pack_half2(p2, p3);
+  // the sum takes the fp16 weights the P.V product uses, so numerator and
+  // denominator weigh every token alike (one dominant token returns its V row)
+  l += sum_half2(pa0) + sum_half2(pa2);
   // ---- rows past the context may hold anything (NaN): zero them, as 0 * NaN
   // would poison the sums -------------------------------------------------------------
   if (valid < kTile) {
@@ -271,9 +275,9 @@ __device__ __forceinline__ void process_tile16(uint32_t st, const uint32_t (&qa)
     }
     const float p0 = exp2_approx(x0 - m[r]), p1 = exp2_approx(x1 - m[r]);
     const float p2 = exp2_approx(x2 - m[r]), p3 = exp2_approx(x3 - m[r]);
-    l[r] += (p0 + p1) + (p2 + p3);
     pa[r] = pack_half2(p0, p1);       // a0 (row r0) / a1 (row r1): tokens 2(lane%4)..
     pa[2 + r] = pack_half2(p2, p3);   // a2 / a3: tokens 8 + 2(lane%4)..
+    l[r] += sum_half2(pa[r]) + sum_half2(pa[2 + r]);   // the fp16 weights, as in P.V
   }
   const int vtok = r8 + ((mi & 1) << 3);
 #pragma unroll

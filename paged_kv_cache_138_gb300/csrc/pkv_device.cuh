@@ -159,6 +159,12 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// lo + hi of a packed half2, in fp32 (exact: both widen exactly).
+__device__ __forceinline__ float sum_half2(uint32_t bits) {
+  const float2 f = half2_to_float2(bits);
+  return f.x + f.y;
+}
+
 __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }

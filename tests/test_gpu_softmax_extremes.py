@@ -123,14 +123,16 @@ def spike_specs(lengths):
     return specs
 
 
-@pytest.mark.parametrize("Hkv,G", [(8, 4), (2, 4), (4, 1)])
+@pytest.mark.parametrize("Hkv,G,v_scale", [(8, 4, 0.4), (2, 4, 0.4), (4, 1, 0.4), (4, 2, 1.0)])
 @pytest.mark.parametrize("fused", [False, True])
-def test_dominant_keys_at_every_boundary(ops, Hkv, G, fused):
+def test_dominant_keys_at_every_boundary(ops, Hkv, G, v_scale, fused):
+    """v_scale 1.0: V rows up to ~4.5 in magnitude, where one dominant token's
+    output must be its V row to within the fp16 output rounding."""
     specs = spike_specs([17, 513, 2049, 4097])
     lengths = [L for L, _ in specs]
     tables, lens, nb = sc.plain_tables(40 + Hkv, lengths)
     q, kc, vc = sc.build(41 + Hkv, tables, lens, [sc.spikes(p) for _, p in specs],
-                         Hq=Hkv * G, Hkv=Hkv, nb=nb, gain_kind="positive")
+                         Hq=Hkv * G, Hkv=Hkv, nb=nb, gain_kind="positive", v_scale=v_scale)
     got, code, dk, dv = run_split(ops, q, kc, vc, tables, lens, fused)
     check(got, kc, vc, q, tables, lens, code, *((dk, dv) if fused else ()))
 
