@@ -214,6 +214,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
                     partition;
   p.shared_splits_cap = shared_splits;
   p.seq_stride = seq_stride_for(num_seqs);
+  p.rank_by_length = num_seqs <= kMaxRankedSeqs && own_splits == 1;
   p.partition_tiles = partition;
   p.scale_log2 = scale * 1.4426950408889634f;
 
