@@ -421,35 +421,59 @@ struct TileStream {
 
 // Combine the 4 warps' (m, l, o) of `rows` query rows held in shared memory
 // (ml [warps][16][2], ob [warps][16][128]) and hand each row's (M, den, num)
-// to emit(row, d, M, den, num) for every output dim d.
+// to emit(row, d, M, den, num4) for dims d .. d + 3.  Warp w takes rows w,
+// w + 4, ...; lane i dims 4 i .. 4 i + 3 (one 16-byte read per warp's
+// partial), so up to 4 rows merge in one pass.  Per element the arithmetic
+// is the warps' weights exp2(m_w - M) in warp order, as one thread per
+// element would do it.
 template <class Emit>
 __device__ __forceinline__ void merge_warps(const float* ml, const float* ob, int rows, Emit&& emit) {
-  for (int e = threadIdx.x; e < rows * kHeadDim; e += kThreads) {
-    const int r = e / kHeadDim, d = e % kHeadDim;
+  const int lane = threadIdx.x & 31;
+  for (int r = threadIdx.x >> 5; r < rows; r += kWarps) {
+    float mw[kWarps];
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * 16 + r) * 2]);
-    float num = 0.f, den = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      mw[w] = ml[(w * 16 + r) * 2];
+      M = fmaxf(M, mw[w]);
+    }
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float c = exp2_approx(ml[(w * 16 + r) * 2] - M);
-        num += c * ob[(w * 16 + r) * kHeadDim + d];
+        const float c = exp2_approx(mw[w] - M);
+        const float4 v = *reinterpret_cast<const float4*>(ob + (w * 16 + r) * kHeadDim + 4 * lane);
+        num.x += c * v.x;
+        num.y += c * v.y;
+        num.z += c * v.z;
+        num.w += c * v.w;
         den += c * ml[(w * 16 + r) * 2 + 1];
       }
     }
-    emit(r, d, M, den, num);
+    emit(r, 4 * lane, M, den, num);
   }
 }
 
 __device__ __forceinline__ void store_partial(const Params& p, int64_t row, int slot, int d,
-                                              float M, float den, float num) {
+                                              float M, float den, float4 num) {
   const int64_t at = row * p.max_splits + slot;
-  p.part_o[at * kHeadDim + d] = num;
+  *reinterpret_cast<float4*>(p.part_o + at * kHeadDim + d) = num;
   if (d == 0) {
     p.part_ml[at * 2] = M;
     p.part_ml[at * 2 + 1] = den;
   }
+}
+
+// fp16 output of dims d .. d + 3 of a row (one 8-byte store)
+__device__ __forceinline__ void store_out4(__half* o, float den, float4 num) {
+  const bool ok = den > 0.f;
+  const __half2 a = __floats2half2_rn(ok ? num.x / den : 0.f, ok ? num.y / den : 0.f);
+  const __half2 b = __floats2half2_rn(ok ? num.z / den : 0.f, ok ? num.w / den : 0.f);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(o) = u;
 }
 
 // Copy-on-write from the staged tile: rows first_row .. first_row + rows - 1
@@ -635,10 +659,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
       *reinterpret_cast<float2*>(orow + nd * 8) = make_float2(o[nd][0], o[nd][1]);
   }
   __syncthreads();
-  merge_warps(ml, ob, G, [&](int gi, int d, float M, float den, float num) {
+  merge_warps(ml, ob, G, [&](int gi, int d, float M, float den, float4 num) {
     const int64_t row = static_cast<int64_t>(s) * Hq + h0 + gi;
     if (nsplit == 1)
-      p.out[row * kHeadDim + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+      store_out4(p.out + row * kHeadDim + d, den, num);
     else
       store_partial(p, row, shared_splits + split, d, M, den, num);
   });
@@ -754,7 +778,7 @@ __device__ __forceinline__ void shared_body(const CUtensorMap& tmap_k, const CUt
     }
   }
   __syncthreads();
-  merge_warps(ml, ob, rows, [&](int r, int d, float M, float den, float num) {
+  merge_warps(ml, ob, rows, [&](int r, int d, float M, float den, float4 num) {
     const int64_t row = static_cast<int64_t>(first + r / G) * Hq + g * G + r % G;
     store_partial(p, row, split, d, M, den, num);
   });

@@ -61,11 +61,7 @@ __global__ void __launch_bounds__(kMergeRows * 32) paged_attention_merge_kernel(
       den += c * ml[2 * i + 1];
     }
   }
-  __half* o = p.out + row * kHeadDim + 4 * lane;
-  o[0] = __float2half_rn(den > 0.f ? num.x / den : 0.f);
-  o[1] = __float2half_rn(den > 0.f ? num.y / den : 0.f);
-  o[2] = __float2half_rn(den > 0.f ? num.z / den : 0.f);
-  o[3] = __float2half_rn(den > 0.f ? num.w / den : 0.f);
+  store_out4(p.out + row * kHeadDim + 4 * lane, den, num);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
