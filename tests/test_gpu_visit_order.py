@@ -2,9 +2,8 @@
 
 Batches of at most 128 sequences whose tables all fit in one split are visited
 in an order computed on the device from the context lengths (longest,
-shortest, second longest, ...); larger batches, or batches whose sequences
-need several splits, take a fixed stride order (grouped launches keep the
-batch order for their own units).  The order must change which
+shortest, second longest, ...); other batches take a fixed stride order
+(grouped launches keep the batch order for their own units).  The order must change which
 CTA runs a sequence and nothing else: every sequence visited exactly once
 (outputs start as NaN), every output equal to the oracle's within the 2e-3
 bound, and a permuted batch giving the permuted outputs bit for bit.
@@ -74,9 +73,10 @@ def lengths_with_ties(seed, S, hi):
 
 
 CASES = [
-    # S, Hq, Hkv, longest context: all one split at these sizes except the
-    # last two (129 sequences; several splits per sequence)
+    # S, Hq, Hkv, longest context: one split per sequence except the last two
+    # (129 sequences; several splits per sequence)
     (5, 8, 8, 63),
+    (24, 24, 24, 512),
     (64, 32, 16, 1024),
     (127, 32, 16, 2048),
     (128, 32, 8, 2048),
@@ -90,7 +90,7 @@ CASES = [
 def test_every_sequence_visited_once(ops, S, Hq, Hkv, hi, fused):
     lens = lengths_with_ties(S * 7 + hi, S, hi)
     q, kc, vc, kn, vn, tables, lens = batch(S + hi, lens, Hq, Hkv)
-    expect_ranked = (S, hi) in {(5, 63), (64, 1024), (127, 2048), (128, 2048)}
+    expect_ranked = (S, hi) in {(5, 63), (24, 512), (64, 1024), (127, 2048), (128, 2048)}
     assert ranked(ops, S, Hkv, tables) == expect_ranked
     got, code, kc_gpu, vc_gpu = run(ops, q, kc, vc, tables, lens, fused, kn, vn)
     assert code == 0
