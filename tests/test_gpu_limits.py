@@ -1,0 +1,119 @@
+"""Attention at the largest sizes a launch accepts, against the fp64 oracle.
+
+* 65,535 sequences: the most one launch takes (the grid's second dimension is
+  the batch); 65,536 is refused with PKV_ERR_UNSUPPORTED before anything runs.
+* One context of 2^20 + 7 tokens: a lone sequence gets 1024-token splits
+  (the longest that still gives 1,024 CTAs), so its row is merged from 1,025
+  partials (the merge's lanes loop over them 33 times), the last split
+  holding 7 tokens.  Three tokens -- in the first
+  split, a middle one and the last -- carry the same dominant key, so the
+  output is close to the mean of their three V rows (O(1), not the ~1e-3
+  average of a million N(0, 1) rows) and a dropped or misweighted split moves
+  it by O(1).
+Tolerance: max |out_gpu - out_oracle| <= 2e-3 on fp16 outputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import cache_ops as oc
+from parity_helpers import attention_tolerance
+from paged_kv_cache_138_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+TOL = attention_tolerance()
+D = 128
+PKV_ERR_UNSUPPORTED = -2
+
+
+@pytest.fixture(scope="module")
+def ops(native_lib):
+    from paged_kv_cache_138_gb300 import ops as o
+    return o
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def many_sequences(seed, S, Hq, Hkv, max_len):
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(1, max_len, S, endpoint=True).astype(np.int32)
+    nb = sum(wl.blocks_for(int(L)) for L in lens) + 1
+    tables = wl.handout_tables(lens, rng.permutation(nb).astype(np.int32))
+    q = wl.host_normal_fp16(rng, (S, Hq, D))
+    kc = wl.host_normal_fp16(rng, (nb, 16, Hkv, D))
+    vc = wl.host_normal_fp16(rng, (nb, 16, Hkv, D))
+    kn = wl.host_normal_fp16(rng, (S, Hkv, D))
+    vn = wl.host_normal_fp16(rng, (S, Hkv, D))
+    return q, kc, vc, kn, vn, tables, lens
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_largest_batch(ops, fused):
+    S, Hq, Hkv = 65535, 8, 1
+    q, kc, vc, kn, vn, tables, lens = many_sequences(65535, S, Hq, Hkv, 32)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    e = ops.new_error_word()
+    kcd, vcd = dev(kc), dev(vc)
+    if fused:
+        ops.paged_attention_decode_fused(out, dev(q), dev(kn), dev(vn), kcd, vcd, dev(tables),
+                                         dev(lens), 1 / np.sqrt(D), dev_err=e)
+        slots = (tables[np.arange(S), (lens - 1) // 16].astype(np.int64) * 16 + (lens - 1) % 16)
+        oc.reshape_and_cache(kn, vn, slots, kc, vc)
+        assert np.array_equal(kcd.cpu().numpy(), kc) and np.array_equal(vcd.cpu().numpy(), vc)
+    else:
+        ops.paged_attention_decode(out, dev(q), kcd, vcd, dev(tables), dev(lens), 1 / np.sqrt(D),
+                                   dev_err=e)
+    assert ops.read_error_word(e) == 0
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
+    assert np.abs(got.astype(np.float64) - ref).max() <= TOL
+
+
+def test_one_sequence_too_many_is_refused(ops):
+    from paged_kv_cache_138_gb300._lib import PagedKVError
+    S, Hq, Hkv = 65536, 8, 1
+    q = torch.zeros(S, Hq, D, dtype=torch.float16, device="cuda")
+    kc = torch.zeros(4, 16, Hkv, D, dtype=torch.float16, device="cuda")
+    tables = torch.zeros(S, 1, dtype=torch.int32, device="cuda")
+    lens = torch.ones(S, dtype=torch.int32, device="cuda")
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    with pytest.raises(PagedKVError) as err:
+        ops.paged_attention_decode(out, q, kc, kc.clone(), tables, lens, 0.1)
+    assert err.value.status == PKV_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()              # nothing was launched
+
+
+@pytest.mark.parametrize("Hq", [1, 8])
+def test_million_token_context(ops, Hq):
+    L = (1 << 20) + 7
+    Hkv = 1
+    rng = np.random.default_rng(L + Hq)
+    nb = wl.blocks_for(L) + 2
+    tables = wl.handout_tables([L], rng.permutation(nb).astype(np.int32))
+    lens = np.array([L], np.int32)
+    q = wl.host_normal_fp16(rng, (1, Hq, D))
+    kc = wl.host_normal_fp16(rng, (nb, 16, Hkv, D))
+    vc = wl.host_normal_fp16(rng, (nb, 16, Hkv, D))
+    # the dominant key: 6 x the sum of the query rows (logit of head h about
+    # 6 (|q_h|^2 + sum_j q_h.q_j) scale = 68 +- 16 against N(0, 1) for the rest)
+    key = (6.0 * q[0].astype(np.float32).sum(axis=0)).astype(np.float16)
+    spots = [5, L // 2 + 3, L - 3]
+    for t in spots:
+        kc[tables[0, t // 16], t % 16, 0] = key
+    assert ops.split_tokens(1, Hkv, tables.shape[1]) == 1024
+    out = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
+    e = ops.new_error_word()
+    ops.paged_attention_decode(out, dev(q), dev(kc), dev(vc), dev(tables), dev(lens),
+                               1 / np.sqrt(D), dev_err=e)
+    assert ops.read_error_word(e) == 0
+    got = out.cpu().numpy().astype(np.float64)
+    ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
+    assert np.isfinite(got).all()
+    assert np.abs(got - ref).max() <= TOL
+    mean3 = np.mean([vc[tables[0, t // 16], t % 16, 0].astype(np.float64) for t in spots], axis=0)
+    assert np.abs(ref - mean3[None, None]).max() < 1e-3   # the three tokens dominate
