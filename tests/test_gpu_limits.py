@@ -10,6 +10,8 @@
   output is close to the mean of their three V rows (O(1), not the ~1e-3
   average of a million N(0, 1) rows) and a dropped or misweighted split moves
   it by O(1).
+* reshape_and_cache of 2^20 tokens filling every slot of a 2^16-block pool,
+  and copy_blocks of 8,000 pairs in 4 layers, bit for bit.
 Tolerance: max |out_gpu - out_oracle| <= 2e-3 on fp16 outputs.
 """
 import numpy as np
@@ -117,3 +119,50 @@ def test_million_token_context(ops, Hq):
     assert np.abs(got - ref).max() <= TOL
     mean3 = np.mean([vc[tables[0, t // 16], t % 16, 0].astype(np.float64) for t in spots], axis=0)
     assert np.abs(ref - mean3[None, None]).max() < 1e-3   # the three tokens dominate
+
+
+def random_bits_fp16(rng, shape):
+    """fp16 arrays of random bit patterns (NaNs and infinities included): the
+    cache kernels move bits, and drawing bytes is far quicker on the host than
+    drawing normals."""
+    n = int(np.prod(shape))
+    return np.frombuffer(rng.bytes(2 * n), dtype=np.float16).reshape(shape).copy()
+
+
+def test_cache_write_of_a_million_tokens(ops):
+    """reshape_and_cache of 2^20 tokens into a pool of exactly 2^16 blocks
+    (every slot written once, in shuffled order, a few skipped with -1), bit
+    for bit against the oracle's scatter."""
+    T, Hkv, nb = 1 << 20, 1, 1 << 16
+    rng = np.random.default_rng(20)
+    k = random_bits_fp16(rng, (T, Hkv, D))
+    v = random_bits_fp16(rng, (T, Hkv, D))
+    slots = rng.permutation(nb * 16).astype(np.int64)
+    slots[rng.choice(T, 5, replace=False)] = -1
+    kc = np.zeros((nb, 16, Hkv, D), np.float16)
+    vc = np.zeros_like(kc)
+    kcd, vcd = dev(kc), dev(vc)
+    e = ops.new_error_word()
+    ops.reshape_and_cache(dev(k), dev(v), dev(slots), kcd, vcd, dev_err=e)
+    assert ops.read_error_word(e) == 0
+    oc.reshape_and_cache(k, v, slots, kc, vc)
+    assert np.array_equal(kcd.cpu().numpy().view(np.uint16), kc.view(np.uint16))
+    assert np.array_equal(vcd.cpu().numpy().view(np.uint16), vc.view(np.uint16))
+
+
+def test_copy_of_eight_thousand_blocks_in_four_layers(ops):
+    """copy_blocks of 8,000 (src, dst) pairs in each of 4 layers, bit for bit
+    against the oracle (so every block outside the destinations unchanged)."""
+    nb, Hkv, layers, P = 20000, 2, 4, 8000
+    rng = np.random.default_rng(21)
+    ids = rng.permutation(nb)
+    pairs = np.stack([ids[:P], ids[P:2 * P]], axis=1).astype(np.int64)
+    kcs = [random_bits_fp16(rng, (nb, 16, Hkv, D)) for _ in range(layers)]
+    vcs = [random_bits_fp16(rng, (nb, 16, Hkv, D)) for _ in range(layers)]
+    kd, vd = [dev(a) for a in kcs], [dev(a) for a in vcs]
+    e = ops.new_error_word()
+    ops.copy_blocks(kd, vd, dev(pairs), dev_err=e)
+    assert ops.read_error_word(e) == 0
+    oc.copy_blocks(kcs, vcs, pairs)
+    for got, ref in zip(kd + vd, kcs + vcs):
+        assert np.array_equal(got.cpu().numpy().view(np.uint16), ref.view(np.uint16))
