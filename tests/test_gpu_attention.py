@@ -13,7 +13,7 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance, oracle_batch
+from parity_helpers import assert_matches_oracle, attention_tolerance, oracle_batch
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -50,9 +50,7 @@ def run_gpu(ops, q, kc, vc, tables, lens, scale, err=None):
 
 
 def assert_close(gpu, ref):
-    err = np.abs(gpu.astype(np.float64) - ref)
-    assert np.isfinite(gpu).all()
-    assert err.max() <= TOL, "max abs error %.3g at %s" % (err.max(), np.unravel_index(err.argmax(), err.shape))
+    assert_matches_oracle(gpu, ref)
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (32, 8), (16, 2), (40, 40)])

@@ -6,7 +6,7 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance
+from parity_helpers import assert_matches_oracle
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -57,9 +57,7 @@ def test_block_sizes_match_oracle(ops, bs, Hq, Hkv):
                                torch.from_numpy(lens).cuda(), scale, dev_err=err)
     assert ops.read_error_word(err) == 0
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, scale)
-    got = out.cpu().numpy().astype(np.float64)
-    assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= attention_tolerance()
+    assert_matches_oracle(out.cpu().numpy(), ref, (bs, Hq, Hkv))
 
 
 @pytest.mark.parametrize("bs", [8, 16, 32, 64])
@@ -81,7 +79,7 @@ def test_fused_cache_write_and_attention(ops, bs, Hq, Hkv):
                      np.int64)
     oc.reshape_and_cache(k_new, v_new, slots, kc, vc)
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
-    assert np.abs(out.cpu().numpy().astype(np.float64) - ref).max() <= attention_tolerance()
+    assert_matches_oracle(out.cpu().numpy(), ref, (bs, Hq, Hkv))
     assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
     assert np.array_equal(dv.cpu().numpy().view(np.uint16), vc.view(np.uint16))
 

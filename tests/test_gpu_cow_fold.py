@@ -16,11 +16,10 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance
+from parity_helpers import assert_matches_oracle
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
-TOL = attention_tolerance()
 D = 128
 SCALE = 1.0 / np.sqrt(D)
 
@@ -107,7 +106,7 @@ def run_case(ops, seed, Hq, Hkv, bs, prompts, samples, prompt_len, earlier, grou
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, SCALE)
     got = out.cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
     return cb, tables, lens
 
 

@@ -6,12 +6,11 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance, oracle_batch
+from parity_helpers import assert_matches_oracle, oracle_batch
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 D = 128
-TOL = attention_tolerance()
 
 
 @pytest.fixture(scope="module")
@@ -72,7 +71,7 @@ def test_grouped_matches_oracle(ops, bs, Hq, Hkv, groups, prefix):
     assert (gs > 0).sum() == sum(1 for m in groups if m > 1)
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
     assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
 
 
 def test_grouped_prefix_sharing_workload(ops):
@@ -87,7 +86,7 @@ def test_grouped_prefix_sharing_workload(ops):
     got, code, gs = run_grouped(ops, q, kc, vc, tables, lens, 16)
     assert code == 0 and list(gs) == [2048] * 8
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, w.scale)
-    assert np.abs(got - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
 
 
 def test_bad_group_is_reported(ops):
@@ -177,7 +176,7 @@ def test_grouped_fused_cache_write_and_attention(ops, bs, Hq, Hkv, groups):
     oc.reshape_and_cache(k_new, v_new, slots, kc, vc)
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
     got = out.cpu().numpy().astype(np.float64)
-    assert np.isfinite(got).all() and np.abs(got - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
     assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
     assert np.array_equal(dv.cpu().numpy().view(np.uint16), vc.view(np.uint16))
 

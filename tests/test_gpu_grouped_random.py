@@ -15,7 +15,7 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance
+from parity_helpers import assert_matches_oracle
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -91,9 +91,7 @@ def test_random_grouped_case_matches_oracle(ops, seed):
                                            dev(sg), dev(gs), mx, mo, scale, dev_err=err)
     assert ops.read_error_word(err) == 0
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, scale)
-    got = out.cpu().numpy().astype(np.float64)
-    assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= attention_tolerance(), (S, Hq, Hkv, bs, fused, list(gs))
+    assert_matches_oracle(out.cpu().numpy(), ref, (S, Hq, Hkv, bs, fused, list(gs)))
     if fused:
         assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
         assert np.array_equal(dv.cpu().numpy().view(np.uint16), vc.view(np.uint16))

@@ -4,7 +4,9 @@ Each case draws the batch size, head counts (G in 1, 2, 4, 8), block size,
 a length mix (uniform, ragged with empty rows, or lengths on block and split
 boundaries) and plain or fused launch, so the launch picks every split length
 and both kinds of grid row order; the output is compared element by element
-(max |GPU - oracle| <= 2e-3) and, for fused launches, the cache bytes too.
+(max |GPU - oracle| <= 2e-3, and in fp16 units of each row's largest value
+a mean of at most 0.25 and a maximum of at most 3) and, for fused launches,
+the cache bytes too.
 """
 import numpy as np
 import pytest
@@ -12,7 +14,7 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance
+from parity_helpers import assert_matches_oracle
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -72,9 +74,7 @@ def test_random_case_matches_oracle(ops, seed):
                                    dev_err=err)
     assert ops.read_error_word(err) == 0
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, scale)
-    got = out.cpu().numpy().astype(np.float64)
-    assert np.isfinite(got).all()
-    assert np.abs(got - ref).max() <= attention_tolerance(), (S, Hq, Hkv, bs, fused)
+    assert_matches_oracle(out.cpu().numpy(), ref, (S, Hq, Hkv, bs, fused))
     if fused:
         assert np.array_equal(dk.cpu().numpy().view(np.uint16), kc.view(np.uint16))
         assert np.array_equal(dv.cpu().numpy().view(np.uint16), vc.view(np.uint16))

@@ -14,11 +14,10 @@ import torch
 
 from oracle import attention as oa
 from oracle import cache_ops as oc
-from parity_helpers import attention_tolerance
+from parity_helpers import assert_matches_oracle
 from paged_kv_cache_138_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
-TOL = attention_tolerance()
 D = 128
 MAX_RANKED = 128
 
@@ -101,7 +100,7 @@ def test_every_sequence_visited_once(ops, S, Hq, Hkv, hi, fused):
         oc.reshape_and_cache(kn, vn, slots, kc, vc)
         assert np.array_equal(kc_gpu, kc) and np.array_equal(vc_gpu, vc)
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
-    assert np.abs(got.astype(np.float64) - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
 
 
 def test_all_lengths_equal_and_empty_rows(ops):
@@ -116,7 +115,7 @@ def test_all_lengths_equal_and_empty_rows(ops):
     assert code == 0
     assert (got[[0, 17, 127]] == 0).all()
     ref = oa.paged_attention_decode(q, kc, vc, tables, lens, 1 / np.sqrt(D))
-    assert np.abs(got.astype(np.float64) - ref).max() <= TOL
+    assert_matches_oracle(got, ref)
 
 
 @pytest.mark.parametrize("S,Hq,Hkv,hi", [(128, 32, 8, 2048), (64, 40, 40, 4096), (200, 8, 8, 600)])
@@ -146,4 +145,4 @@ def test_bad_length_in_a_ranked_batch_is_reported(ops):
     assert code == 2                           # PKV_DEV_BAD_CONTEXT_LEN
     keep = [s for s in range(S) if s not in (3, 40)]
     ref = oa.paged_attention_decode(q[keep], kc, vc, tables[keep], lens[keep], 1 / np.sqrt(D))
-    assert np.abs(got[keep].astype(np.float64) - ref).max() <= TOL
+    assert_matches_oracle(got[keep], ref)
