@@ -129,6 +129,12 @@ struct pkv_block_manager {
   }
 };
 
+namespace {
+int check_invariants(const pkv_block_manager& bm);
+int cow_targets(const int64_t* pairs, int num_pairs, const int32_t* tables, int num_seqs,
+                int max_blocks, int32_t* cow_block, int32_t* cow_src);
+}  // namespace
+
 extern "C" {
 
 pkv_block_manager* pkv_bm_create(int64_t num_blocks, int block_size, int enable_prefix_cache,
@@ -298,17 +304,21 @@ int pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id) {
 
 int pkv_bm_free(pkv_block_manager* bm, int64_t seq_id) {
   if (!bm) return PKV_ERR_INVALID_ARG;
-  auto it = bm->seqs.find(seq_id);
-  if (it == bm->seqs.end()) return PKV_OK;
-  const std::vector<int32_t>& table = it->second.table;
-  for (auto b = table.rbegin(); b != table.rend(); ++b) {
-    if (--bm->ref[*b] == 0) {
-      if (bm->hashed[*b]) bm->ev_push_back(*b);  // newest end of the LRU pool
-      else bm->free_list.push_back(*b);
+  try {
+    auto it = bm->seqs.find(seq_id);
+    if (it == bm->seqs.end()) return PKV_OK;
+    const std::vector<int32_t>& table = it->second.table;
+    for (auto b = table.rbegin(); b != table.rend(); ++b) {
+      if (--bm->ref[*b] == 0) {
+        if (bm->hashed[*b]) bm->ev_push_back(*b);  // newest end of the LRU pool
+        else bm->free_list.push_back(*b);          // (may allocate)
+      }
     }
+    bm->seqs.erase(it);
+    return PKV_OK;
+  } catch (...) {  // the free list could not grow: no exception crosses the C ABI
+    return PKV_ERR_INVALID_ARG;
   }
-  bm->seqs.erase(it);
-  return PKV_OK;
 }
 
 int pkv_bm_slot(const pkv_block_manager* bm, int64_t seq_id, int64_t pos, int64_t* slot_out) {
@@ -416,6 +426,18 @@ int64_t pkv_bm_ref_counts(const pkv_block_manager* bm, int32_t* out, int64_t cap
 
 int pkv_bm_check_invariants(const pkv_block_manager* bm) {
   if (!bm) return PKV_ERR_INVALID_ARG;
+  try {
+    return check_invariants(*bm);
+  } catch (...) {  // scratch arrays could not be allocated
+    return PKV_ERR_INVALID_ARG;
+  }
+}
+
+}  // extern "C"
+
+namespace {
+int check_invariants(const pkv_block_manager& bmr) {
+  const pkv_block_manager* bm = &bmr;
   const int64_t nb = bm->num_blocks;
   std::vector<uint8_t> in_free(static_cast<size_t>(nb), 0);
   for (int32_t b : bm->free_list) {
@@ -447,8 +469,7 @@ int pkv_bm_check_invariants(const pkv_block_manager* bm) {
   }
   return 0;
 }
-
-}  // extern "C"
+}  // namespace
 
 // ---- shared-prefix group planning (host) -----------------------------------------
 // Consecutive sequences whose tables start with the same physical block form a
@@ -519,6 +540,16 @@ extern "C" int pkv_cow_targets(const int64_t* pairs, int num_pairs, const int32_
   if (num_seqs > 0 && (!tables || !cow_block || !cow_src)) return PKV_ERR_INVALID_ARG;
   if (num_pairs > 0 && !pairs) return PKV_ERR_INVALID_ARG;
   for (int s = 0; s < num_seqs; ++s) cow_block[s] = cow_src[s] = -1;
+  try {
+    return cow_targets(pairs, num_pairs, tables, num_seqs, max_blocks, cow_block, cow_src);
+  } catch (...) {  // the lookup table could not be allocated
+    return PKV_ERR_INVALID_ARG;
+  }
+}
+
+namespace {
+int cow_targets(const int64_t* pairs, int num_pairs, const int32_t* tables, int num_seqs,
+                int max_blocks, int32_t* cow_block, int32_t* cow_src) {
   struct Target {
     int64_t src;
     int hits;
@@ -550,3 +581,4 @@ extern "C" int pkv_cow_targets(const int64_t* pairs, int num_pairs, const int32_
     if (kv.second.hits != 1) return PKV_ERR_BAD_INDEX;  // in no table, or in two places
   return two_in_one ? PKV_ERR_UNSUPPORTED : PKV_OK;
 }
+}  // namespace
