@@ -11,7 +11,6 @@ concatenate them, slice to the context length and apply dense softmax attention.
 The two forms share no code; tests require them to agree to 1e-12.
 """
 import ctypes
-import os
 
 import numpy as np
 

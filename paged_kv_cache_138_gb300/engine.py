@@ -8,7 +8,6 @@ the C ABI; ``run_from_host()`` is the same step fed from pinned host buffers,
 with the host->device copies of the inputs and the device->host copy of the
 output inside it.
 """
-import numpy as np
 import torch
 
 from . import ops
