@@ -92,9 +92,10 @@ int pkv_version(void);
  * split) >= 1024 CTAs; their partials are merged by log-sum-exp.  A
  * sequence's output bits therefore depend on its own length and on those
  * launch sizes only: not on block ids, the order of the batch or the other
- * sequences' lengths.  (A batch of at most 128 sequences whose tables all fit
- * in one split is visited on the device longest, shortest, second longest,
- * ... by context_lens; that changes which CTA runs a sequence, never the
+ * sequences' lengths.  (In a batch of at most 128 sequences whose last
+ * split can be at least half a split long -- by the table width -- the last
+ * split of each sequence is visited on the device longest, shortest, second
+ * longest, ... by context_lens; that changes which CTA runs a unit, never the
  * arithmetic.)
  */
 int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,

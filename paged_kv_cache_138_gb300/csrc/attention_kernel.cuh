@@ -99,7 +99,7 @@ struct Params {
   int own_tiles_cap;  // grouped launches: own tiles the grid covers per sequence
   int shared_splits_cap;  // grouped launches: split slots reserved for a shared prefix
   int seq_stride;     // split grid: row y of the grid is sequence (y * seq_stride) % S
-  int rank_by_length;  // split grid: visit sequences in zigzag_rank order of length
+  int rank_by_length;  // split grid: last split plane in zigzag_rank order of length
   int partition_tiles;  // T: tiles per split (32, 64 or 128)
   float scale_log2;
 };
@@ -833,22 +833,25 @@ __device__ __forceinline__ int zigzag_rank(int y, int n) {
 }
 
 // grid (KV heads, sequences, splits).  CTAs start in grid order (all first
-// splits, then all second splits, ...).  Two orders of the rows:
-//  * rank_by_length (at most kMaxRankedSeqs sequences, each one unit: no
-//    table is longer than one split): rows alternate between the longest and
-//    the shortest sequences not yet visited (zigzag_rank), so long units
-//    start first, every short unit's set-up and merge run beside a long
-//    unit's streaming, and the grid ends on units of median length: the last
-//    wave, where SMs fall idle one by one, holds neither the longest work nor
-//    a crowd of short, latency-bound units (longest first alone measured
-//    -5.5 % on a batch of many very short sequences).  With several splits per
-//    sequence the split planes already start every long sequence's
-//    full-length units first; ranking measured no gain there;
-//  * otherwise row y takes sequence (y * seq_stride) % S, a stride coprime
-//    with S near 0.618 S: a batch ordered by length (as continuous batching
-//    tends to keep it: older requests are longer) would otherwise start all
-//    its short units back to back, and a CTA with a short unit spends most of
-//    its life in set-up and merge.
+// splits, then all second splits, ...), so the last split plane makes the
+// last waves, where SMs fall idle one by one.  Two orders of the rows:
+//  * rank_by_length (at most kMaxRankedSeqs sequences, and a last plane whose
+//    units can reach half a split: the host checks the table width), on the
+//    last plane only: rows alternate between the longest and the shortest
+//    sequences not yet visited (zigzag_rank), so long units start first,
+//    every short unit's set-up and merge run beside a long unit's streaming,
+//    and the grid ends on units of median length rather than on a random
+//    long one or a crowd of short, latency-bound ones (longest first alone
+//    measured -5.5 % on a batch of many very short sequences).  Ranking every
+//    plane measured slower on batches with several splits (each CTA's ranking
+//    delays its first load, and the earlier planes' units are mostly whole
+//    splits anyway), as did ranking a last plane of short remainders;
+//  * every other plane, and every plane of other batches: row y takes
+//    sequence (y * seq_stride) % S, a stride coprime with S near 0.618 S: a
+//    batch ordered by length (as continuous batching tends to keep it: older
+//    requests are longer) would otherwise start all its short units back to
+//    back, and a CTA with a short unit spends most of its life in set-up and
+//    merge.
 template <int G, int BS, bool FUSED>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_attention_split_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -860,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   uint8_t* smem = aligned_smem();
   const int y = blockIdx.y;
-  const int s = p.rank_by_length
+  const int s = (p.rank_by_length && blockIdx.z == gridDim.z - 1)
                     ? ranked_sequence(p, smem, zigzag_rank(y, p.num_seqs))
                     : static_cast<int>(static_cast<int64_t>(y) * p.seq_stride % p.num_seqs);
   split_body<G, BS, FUSED>(tmap_k, tmap_v, p, smem, blockIdx.x, s, blockIdx.z);

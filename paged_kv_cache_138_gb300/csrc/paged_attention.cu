@@ -210,7 +210,15 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
                     partition;
   p.shared_splits_cap = shared_splits;
   p.seq_stride = seq_stride_for(num_seqs);
-  p.rank_by_length = num_seqs <= kMaxRankedSeqs && own_splits == 1;
+  {
+    // the last split plane is visited in zigzag order of length when its
+    // units can reach half a split (shorter remainders do not shape the tail)
+    const int64_t table_tiles =
+        tiles_for_tokens(static_cast<int64_t>(max_blocks_per_seq) * block_size);
+    const int64_t last_plane_tiles =
+        table_tiles - static_cast<int64_t>(own_splits - 1) * partition;
+    p.rank_by_length = num_seqs <= kMaxRankedSeqs && 2 * last_plane_tiles >= partition;
+  }
   p.partition_tiles = partition;
   p.scale_log2 = scale * 1.4426950408889634f;
 

@@ -1,8 +1,9 @@
 """The order in which a launch visits the sequences of a batch.
 
-Batches of at most 128 sequences whose tables all fit in one split are visited
-in an order computed on the device from the context lengths (longest,
-shortest, second longest, ...); other batches take a fixed stride order
+In batches of at most 128 sequences whose last split can be at least half a
+split long (by the table width), the last split plane is visited in an order
+computed on the device from the context lengths (longest, shortest, second
+longest, ...); other planes and other batches take a fixed stride order
 (grouped launches keep the batch order for their own units).  The order must change which
 CTA runs a sequence and nothing else: every sequence visited exactly once
 (outputs start as NaN), every output equal to the oracle's within the 2e-3
@@ -43,8 +44,13 @@ def batch(seed, lengths, Hq, Hkv):
 
 
 def ranked(ops, S, Hkv, tables):
-    """Whether a launch of these sizes takes the length-ranked order."""
-    return S <= MAX_RANKED and tables.shape[1] * 16 <= ops.split_tokens(S, Hkv, tables.shape[1])
+    """Whether a launch of these sizes visits its last split plane in the
+    length-ranked order (block size 16: one tile per block)."""
+    split_tiles = ops.split_tokens(S, Hkv, tables.shape[1]) // 16
+    table_tiles = tables.shape[1]
+    planes = -(-table_tiles // split_tiles)
+    last = table_tiles - (planes - 1) * split_tiles
+    return S <= MAX_RANKED and 2 * last >= split_tiles
 
 
 def run(ops, q, kc, vc, tables, lens, fused=False, kn=None, vn=None):
@@ -72,8 +78,9 @@ def lengths_with_ties(seed, S, hi):
 
 
 CASES = [
-    # S, Hq, Hkv, longest context: one split per sequence except the last two
-    # (129 sequences; several splits per sequence)
+    # S, Hq, Hkv, longest context.  Ranked: the 24- to 128-sequence batches
+    # (one split per sequence) and 64 x 4096 (two splits: the second plane).
+    # Not ranked: 5 sequences (units far shorter than a split), 129 sequences.
     (5, 8, 8, 63),
     (24, 24, 24, 512),
     (64, 32, 16, 1024),
@@ -89,7 +96,7 @@ CASES = [
 def test_every_sequence_visited_once(ops, S, Hq, Hkv, hi, fused):
     lens = lengths_with_ties(S * 7 + hi, S, hi)
     q, kc, vc, kn, vn, tables, lens = batch(S + hi, lens, Hq, Hkv)
-    expect_ranked = (S, hi) in {(5, 63), (24, 512), (64, 1024), (127, 2048), (128, 2048)}
+    expect_ranked = (S, hi) in {(24, 512), (64, 1024), (127, 2048), (128, 2048), (64, 4096)}
     assert ranked(ops, S, Hkv, tables) == expect_ranked
     got, code, kc_gpu, vc_gpu = run(ops, q, kc, vc, tables, lens, fused, kn, vn)
     assert code == 0
@@ -107,7 +114,7 @@ def test_all_lengths_equal_and_empty_rows(ops):
     """Every length tied (the order is then the batch order) and rows of
     length 0 among them, in a ranked batch."""
     S, Hq, Hkv = 128, 32, 8
-    lens = np.full(S, 700, np.int32)
+    lens = np.full(S, 1500, np.int32)
     lens[[0, 17, 127]] = 0
     q, kc, vc, _, _, tables, lens = batch(91, lens, Hq, Hkv)
     assert ranked(ops, S, Hkv, tables)
@@ -134,7 +141,8 @@ def test_bad_length_in_a_ranked_batch_is_reported(ops):
     """A negative and an oversized context length among ranked sequences: the
     error word says so and every other sequence is still right."""
     S, Hq, Hkv = 64, 16, 16
-    lens = np.random.default_rng(4).integers(1, 1024, S, endpoint=True).astype(np.int32)
+    lens = np.random.default_rng(4).integers(1, 2048, S, endpoint=True).astype(np.int32)
+    lens[0] = 2048
     q, kc, vc, _, _, tables, lens = batch(44, lens, Hq, Hkv)
     assert ranked(ops, S, Hkv, tables)
     bad = lens.copy()
