@@ -254,10 +254,18 @@ int pkv_paged_attention_decode_grouped_fused(
  * The block must hold some of the sequence's own tokens (below
  * context_lens[s], past a group's shared prefix), else PKV_DEV_BAD_POSITION;
  * a source or table entry outside [0, num_blocks) gives PKV_DEV_BAD_BLOCK_ID;
- * either way no copy is made for s.  block_size must be 8 or 16
- * (PKV_ERR_UNSUPPORTED otherwise: larger blocks span several tiles).  Other
- * arguments, layouts and errors as pkv_paged_attention_decode_fused /
- * pkv_paged_attention_decode_grouped_fused.
+ * either way no copy is made for s.  Every block size the attention entry
+ * points take (8, 16, 32, 64): a block of 32 or 64 rows is staged by 2 or 4
+ * tiles, each storing its rows, and the rows past the context's last tile are
+ * copied from the source by the unit holding that tile.
+ * The pages' order is copy, then write.  Within one launch a copy takes the
+ * source's rows while other sequences of the launch may write new tokens into
+ * that source; so no other sequence may write its new token into a copied
+ * source block at a row other than the copying sequence's own new-token row
+ * (that row the copy replaces with its own token).  The BlockManager's fork
+ * gives every sample of a prompt the same length, so their first writes fall
+ * on one row.  Other arguments, layouts and errors as
+ * pkv_paged_attention_decode_fused / pkv_paged_attention_decode_grouped_fused.
  */
 int pkv_paged_attention_decode_fused_cow(
     void* out, const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,

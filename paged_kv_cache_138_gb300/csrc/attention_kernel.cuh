@@ -476,15 +476,16 @@ __device__ __forceinline__ void store_out4(__half* o, float den, float4 num) {
   *reinterpret_cast<uint2*>(o) = u;
 }
 
-// Copy-on-write from the staged tile: rows first_row .. first_row + rows - 1
-// of the stage (K and V of KV head g, the whole source block: rows = BS <=
-// 16) are stored as block `dst`, one 16-byte chunk per lane and step; the
-// half-warps write 256 contiguous bytes each.
+// Copy-on-write from the staged tile: staged rows first_row .. first_row +
+// rows - 1 (K and V of KV head g) are stored as rows dst_row .. dst_row +
+// rows - 1 of block `dst`, one 16-byte chunk per lane and step; the
+// half-warps write 256 contiguous bytes each.  A block of at most 16 rows is
+// staged whole by one tile; a longer one by one tile per 16 rows.
 template <int BS>
-__device__ __forceinline__ void store_staged_block(uint32_t st, const Params& p, int g,
-                                                   int32_t dst, int first_row, int lane) {
-  static_assert(BS <= kTile, "a copied block must fit in one tile");
-  for (int i = lane; i < BS * 32; i += 32) {
+__device__ __forceinline__ void store_staged_rows(uint32_t st, const Params& p, int g,
+                                                  int32_t dst, int first_row, int dst_row,
+                                                  int rows, int lane) {
+  for (int i = lane; i < rows * 32; i += 32) {
     const int r = i >> 5, c = i & 15;
     const bool is_v = (i >> 4) & 1;
     uint4 val;
@@ -492,10 +493,27 @@ __device__ __forceinline__ void store_staged_block(uint32_t st, const Params& p,
                  : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
                  : "r"(tile_chunk(st, is_v ? 2 : 0, first_row + r, c)));
     const int64_t at =
-        ((static_cast<int64_t>(dst) * BS + r) * p.num_kv_heads + g) * kHeadDim + c * 8;
+        ((static_cast<int64_t>(dst) * BS + dst_row + r) * p.num_kv_heads + g) * kHeadDim + c * 8;
     *reinterpret_cast<uint4*>((is_v ? p.v_cache : p.k_cache) + at) = val;
   }
   __syncwarp();  // every lane has read the stage before it changes again
+}
+
+// Copy-on-write of the rows of a block past every tile the launch streams
+// (a block longer than 16 rows whose last rows lie past the context): rows
+// from_row .. BS - 1 of block `src`, K and V of KV head g, copied to block
+// `dst` with 16-byte loads and stores.
+template <int BS>
+__device__ __forceinline__ void copy_block_tail(const Params& p, int g, int32_t src, int32_t dst,
+                                                int from_row, int lane) {
+  const int64_t block_elems = static_cast<int64_t>(BS) * p.num_kv_heads * kHeadDim;
+  for (int i = lane; i < (BS - from_row) * 32; i += 32) {
+    const int r = from_row + (i >> 5), c = i & 15;
+    __half* base = ((i >> 4) & 1) ? p.v_cache : p.k_cache;
+    const int64_t off = (static_cast<int64_t>(r) * p.num_kv_heads + g) * kHeadDim + c * 8;
+    const uint4 val = *reinterpret_cast<const uint4*>(base + src * block_elems + off);
+    *reinterpret_cast<uint4*>(base + dst * block_elems + off) = val;
+  }
 }
 
 // One CTA per (KV head, sequence, split of its own tiles).  In grouped launches
@@ -544,12 +562,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
   if (tile_begin >= ntiles) return;
   const int n_here = min(p.partition_tiles, ntiles - tile_begin);
 
-  // copy-on-write folded into the launch (FUSED, BS <= 16): the block must
-  // hold some of the sequence's own tokens; the unit whose tile holds it reads
-  // the source block instead and stores the staged rows as the block
-  int cow_blk = -1, cow_tile = -1;
+  // copy-on-write folded into the launch (FUSED): the block must hold some
+  // of the sequence's own tokens; the units whose tiles hold it read the
+  // source block instead and store the staged rows as the block's (tiles
+  // cow_tile_lo .. cow_tile_hi; one tile for BS <= 16)
+  int cow_blk = -1, cow_tile_lo = -1, cow_tile_hi = -2;
   int32_t cow_from = -1, cow_to = -1;
-  if constexpr (FUSED && BS <= kTile) {
+  if constexpr (FUSED) {
     if (p.cow_block) {
       const int cb = __ldg(p.cow_block + s);
       if (cb >= 0) {
@@ -563,7 +582,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
             if (may_report) report(p.dev_err, PKV_DEV_BAD_BLOCK_ID);
           } else {
             cow_blk = cb;
-            cow_tile = cb * BS / kTile;
+            cow_tile_lo = cb * BS / kTile;
+            cow_tile_hi = (cb * BS + BS - 1) / kTile;
             cow_from = from;
             cow_to = to;
           }
@@ -613,7 +633,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
       // cache write of the new token: global slot and the staged row (a
       // block being copied is written at its copy, not at its source)
       int32_t blk = (BS < kTile && new_row >= BS) ? t.b : t.a;
-      if (tile == cow_tile && (L - 1) / BS == cow_blk) blk = cow_to;
+      if ((L - 1) / BS == cow_blk) blk = cow_to;
       const int row_in_block = (L - 1) % BS;
       const int c = lane & 15;
       const bool is_v = lane >= 16;
@@ -629,11 +649,21 @@ __device__ __forceinline__ void split_body(const CUtensorMap& tmap_k, const CUte
       fence_proxy_async_smem();
       __syncwarp();
     }
-    if constexpr (FUSED && BS <= kTile) {
+    if constexpr (FUSED) {
       // the copied block, new token included, before process_tile zeroes the
       // V rows past the context in the stage
-      if (tile == cow_tile)
-        store_staged_block<BS>(st, p, g, cow_to, (cow_blk * BS) % kTile, lane);
+      if (tile >= cow_tile_lo && tile <= cow_tile_hi) {
+        if constexpr (BS <= kTile) {
+          store_staged_rows<BS>(st, p, g, cow_to, (cow_blk * BS) % kTile, 0, BS, lane);
+        } else {
+          const int dst_row = tile * kTile - cow_blk * BS;
+          store_staged_rows<BS>(st, p, g, cow_to, 0, dst_row, kTile, lane);
+          // the context's last tile: the block's rows past it are streamed
+          // by no unit, so this one copies them from the source
+          if (tile == (L - 1) / kTile && dst_row + kTile < BS)
+            copy_block_tail<BS>(p, g, cow_from, cow_to, dst_row + kTile, lane);
+        }
+      }
     }
     process_tile(st, qa, min(kTile, L - tile * kTile), lane, p.scale_log2, m, l, o);
   });

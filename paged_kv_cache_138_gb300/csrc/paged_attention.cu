@@ -146,8 +146,6 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
   if (fused && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
   if ((cow_block != nullptr) != (cow_src != nullptr) || (cow_block && !fused))
     return PKV_ERR_INVALID_ARG;
-  // a copied block is staged whole by one tile only for block sizes <= 16
-  if (cow_block && block_size > kTile) return PKV_ERR_UNSUPPORTED;
   const uintptr_t align = reinterpret_cast<uintptr_t>(k_cache) |
                           reinterpret_cast<uintptr_t>(v_cache) |
                           reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new);

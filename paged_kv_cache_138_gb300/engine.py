@@ -62,10 +62,10 @@ class DecodeStep:
         self.slot_mapping = torch.from_numpy(batch.slot_mapping).to(dev)
         self.cow_pairs = torch.from_numpy(batch.cow_pairs).to(dev)
         # fused steps make the copy-on-write copies inside each layer's
-        # attention launch (one copy per sequence, block size <= 16); others,
-        # or a sequence needing two copies in one step, use copy_blocks
+        # attention launch (one copy per sequence); others, or a sequence
+        # needing two copies in one step, use copy_blocks
         self.cow = None
-        if self.fused and batch.cow_pairs.shape[0] and bs <= 16 and fold_cow:
+        if self.fused and batch.cow_pairs.shape[0] and fold_cow:
             try:
                 cb, cs = ops.cow_targets(batch.cow_pairs, batch.block_tables)
                 self.cow = (torch.from_numpy(cb).to(dev), torch.from_numpy(cs).to(dev))

@@ -6,9 +6,11 @@ Forked samples share a prompt whose last block is partial; a sample that
 appends writes into its own copy of that block ("ans20xx day 31", fork and
 copy-on-write).  The cases cover the copy being the block the new token goes
 into (the copy must carry the token) and an earlier block, block sizes 8
-(either half of a 16-row tile) and 16, grouped and plain launches; every copy
-destination holds NaN before the launch, so a row the kernel fails to copy
-shows.  Caches are compared bit for bit, outputs within 2e-3.
+(either half of a 16-row tile), 16, 32 and 64 (a block staged by 2 or 4
+tiles, the rows past the context copied from the source), grouped and plain
+launches; every copy destination holds NaN before the launch, so a row the
+kernel fails to copy shows.  Caches are compared bit for bit, outputs with
+the parity measure.
 """
 import numpy as np
 import pytest
@@ -40,7 +42,11 @@ def forked_with_cow(seed, prompts, samples, prompt_len, bs, Hkv, own_max, earlie
     copy (dst) of it, sample 0 keeps the shared block (reference count 1 once
     the others copied).  With earlier=True every sample then holds own_max
     more tokens, so the copied block is no longer the one the new token goes
-    into.  Returns tables, lens, nb, pairs (src, dst)."""
+    into; sample 0's run past the shared block, since a launch that copies a
+    block must not also write another sequence's new token into that source
+    at a row the copies take (the pages' order is copy, then write; a fork
+    gives every sample one length, so their first writes share one row).
+    Returns tables, lens, nb, pairs (src, dst)."""
     rng = np.random.default_rng(seed)
     pb = wl.blocks_for(prompt_len, bs)
     rows, lens, pairs, nxt = [], [], [], 0
@@ -54,6 +60,8 @@ def forked_with_cow(seed, prompts, samples, prompt_len, bs, Hkv, own_max, earlie
                 row[-1] = nxt
                 nxt += 1
             extra = int(rng.integers(1, own_max + 1)) if earlier else 1
+            if earlier and k == 0:              # its new token past the shared block
+                extra = max(extra, pb * bs - prompt_len + 1)
             L = prompt_len + extra
             need = wl.blocks_for(L, bs) - len(row)
             row += list(range(nxt, nxt + need))
@@ -110,14 +118,16 @@ def run_case(ops, seed, Hq, Hkv, bs, prompts, samples, prompt_len, earlier, grou
     return cb, tables, lens
 
 
-@pytest.mark.parametrize("bs", [8, 16])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
 @pytest.mark.parametrize("Hq,Hkv", [(8, 8), (16, 4)])
 @pytest.mark.parametrize("earlier", [False, True])
 @pytest.mark.parametrize("grouped", [False, True])
 def test_folded_copy_matches_copy_blocks_then_attention(ops, bs, Hq, Hkv, earlier, grouped):
     samples = 16 // (Hq // Hkv)
     # prompt lengths whose last block is partial, at both halves of a tile
-    for prompt_len in (1000 + 3, 1000 + 11):
+    # and (block sizes 32, 64) in the block's first, middle and last tile
+    lens = (1000 + 3, 1000 + 11) if bs <= 16 else (1024 + 3, 1024 + 20, 1024 + bs - 5)
+    for prompt_len in lens:
         cb, tables, lens = run_case(ops, prompt_len + bs + Hq, Hq, Hkv, bs, 3, samples,
                                     prompt_len, earlier, grouped)
         new_block = (lens - 1) // bs
@@ -154,11 +164,3 @@ def test_bad_copy_metadata_is_reported(ops):
         ops.paged_attention_decode_fused(out, q, kn, kn, kc, kc.clone(), dev(tables), dev(lens),
                                          SCALE, dev_err=err, cow=(dev(b), dev(c)))
         assert ops.read_error_word(err) == code, bad
-    # block sizes past 16 are refused before anything is launched
-    from paged_kv_cache_138_gb300._lib import PagedKVError
-    kc32 = torch.zeros((8, 32, 8, D), dtype=torch.float16, device="cuda")
-    t32 = torch.zeros((S, 8), dtype=torch.int32, device="cuda")
-    with pytest.raises(PagedKVError) as e:
-        ops.paged_attention_decode_fused(out, q, kn, kn, kc32, kc32, t32, dev(lens), SCALE,
-                                         cow=(dev(cb), dev(cs)))
-    assert e.value.status == -2
