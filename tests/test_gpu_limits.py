@@ -12,6 +12,7 @@
   it by O(1).
 * reshape_and_cache of 2^20 tokens filling every slot of a 2^16-block pool,
   and copy_blocks of 8,000 pairs in 4 layers, bit for bit.
+* The empty cases: no sequences, no tokens, no pairs.
 Tolerance: max |out_gpu - out_oracle| <= 2e-3 on fp16 outputs.
 """
 import numpy as np
@@ -165,3 +166,26 @@ def test_copy_of_eight_thousand_blocks_in_four_layers(ops):
     oc.copy_blocks(kcs, vcs, pairs)
     for got, ref in zip(kd + vd, kcs + vcs):
         assert np.array_equal(got.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+
+
+def test_empty_calls_return_ok_and_touch_nothing(ops):
+    """No sequences, no tokens, no pairs: every entry point returns OK,
+    reports nothing and leaves the caches as they were."""
+    Hq, Hkv, nb = 8, 2, 4
+    kc = torch.randn(nb, 16, Hkv, D, device="cuda").half()
+    vc = torch.randn(nb, 16, Hkv, D, device="cuda").half()
+    k0, v0 = kc.clone(), vc.clone()
+    q = torch.empty(0, Hq, D, dtype=torch.float16, device="cuda")
+    kn = torch.empty(0, Hkv, D, dtype=torch.float16, device="cuda")
+    out = torch.empty(0, Hq, D, dtype=torch.float16, device="cuda")
+    tables = torch.empty(0, 3, dtype=torch.int32, device="cuda")
+    lens = torch.empty(0, dtype=torch.int32, device="cuda")
+    e = ops.new_error_word()
+    ops.paged_attention_decode(out, q, kc, vc, tables, lens, 0.1, dev_err=e)
+    ops.paged_attention_decode_fused(out, q, kn, kn.clone(), kc, vc, tables, lens, 0.1, dev_err=e)
+    ops.reshape_and_cache(kn, kn.clone(), torch.empty(0, dtype=torch.int64, device="cuda"), kc, vc,
+                          dev_err=e)
+    ops.copy_blocks(kc, vc, torch.empty(0, 2, dtype=torch.int64, device="cuda"), dev_err=e)
+    torch.cuda.synchronize()
+    assert ops.read_error_word(e) == 0
+    assert torch.equal(kc, k0) and torch.equal(vc, v0)
