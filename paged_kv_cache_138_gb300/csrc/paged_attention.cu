@@ -231,9 +231,7 @@ int decode(void* out, const void* q, const void* k_new, const void* v_new, const
     // prefix (a sequence outside any group counts all its tokens as its own)
     const int own = (tiles_for_tokens(groups.max_own_tokens) + partition - 1) / partition;
     // spread the shared units over the first half of the grid when own units
-    // are at most half as long (measured on forked samples: +3 %; over the
-    // whole grid -9 %, the last long units finishing alone; over the first
-    // third -0.2 %); else first
+    // are at most half as long (measured on forked samples: +3 %); else first
     const int64_t n_shared = static_cast<int64_t>(num_kv_heads) * groups.num_groups * shared_splits;
     const int64_t n_total = n_shared + static_cast<int64_t>(num_kv_heads) * num_seqs * own;
     int stride = 1;
