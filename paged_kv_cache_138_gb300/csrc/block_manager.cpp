@@ -346,7 +346,8 @@ int64_t pkv_bm_block_table(const pkv_block_manager* bm, int64_t seq_id, int32_t*
   if (it == bm->seqs.end()) return PKV_ERR_BAD_INDEX;
   const std::vector<int32_t>& t = it->second.table;
   const int64_t n = static_cast<int64_t>(t.size());
-  if (out) std::memcpy(out, t.data(), sizeof(int32_t) * static_cast<size_t>(n < cap ? n : cap));
+  const int64_t k = std::max<int64_t>(0, std::min(n, cap));  // a negative cap copies nothing
+  if (out && k > 0) std::memcpy(out, t.data(), sizeof(int32_t) * static_cast<size_t>(k));
   return n;
 }
 
@@ -420,7 +421,8 @@ int64_t pkv_bm_evictable_list(const pkv_block_manager* bm, int32_t* out, int64_t
 int64_t pkv_bm_ref_counts(const pkv_block_manager* bm, int32_t* out, int64_t cap) {
   if (!bm) return PKV_ERR_INVALID_ARG;
   const int64_t n = bm->num_blocks;
-  if (out) std::memcpy(out, bm->ref.data(), sizeof(int32_t) * static_cast<size_t>(n < cap ? n : cap));
+  const int64_t k = std::max<int64_t>(0, std::min(n, cap));  // a negative cap copies nothing
+  if (out && k > 0) std::memcpy(out, bm->ref.data(), sizeof(int32_t) * static_cast<size_t>(k));
   return n;
 }
 

@@ -135,7 +135,9 @@ int64_t pkv_sched_request_tokens(const pkv_scheduler* s, int64_t rid, int32_t* o
   auto it = s->reqs.find(rid);
   if (it == s->reqs.end()) return PKV_ERR_BAD_INDEX;
   const int64_t n = static_cast<int64_t>(it->second.tokens.size());
-  if (out) std::memcpy(out, it->second.tokens.data(), sizeof(int32_t) * static_cast<size_t>(std::min(n, cap)));
+  const int64_t k = std::max<int64_t>(0, std::min(n, cap));  // a negative cap copies nothing
+  if (out && k > 0)
+    std::memcpy(out, it->second.tokens.data(), sizeof(int32_t) * static_cast<size_t>(k));
   return n;
 }
 

@@ -145,3 +145,20 @@ def test_utilization_follows_the_allocator_formula(bm_mod):
         assert bm.utilization == pytest.approx(0.5)
         bm.free(2)
         assert bm.utilization == 0.0
+
+
+def test_negative_capacity_copies_nothing(bm_mod):
+    """The C ABI's copy-out calls take a capacity; a negative one copies
+    nothing (the count is still returned)."""
+    import ctypes
+    import numpy as np
+    from paged_kv_cache_138_gb300._lib import lib
+    bm = bm_mod.BlockManager(8, 2, True)
+    bm.allocate(1, [1, 2, 3, 4, 5])
+    out = np.full(8, -7, dtype=np.int32)
+    p = out.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert lib().pkv_bm_block_table(bm._h, 1, p, -1) == 3
+    assert lib().pkv_bm_ref_counts(bm._h, p, -5) == 8
+    assert (out == -7).all()
+    assert lib().pkv_bm_block_table(bm._h, 1, p, 2) == 3
+    assert list(out[:3]) == list(bm.block_table(1)[:2]) + [-7]

@@ -163,3 +163,21 @@ def test_native_scheduler_matches_reference_policy(native_lib, swap):
     assert preempted > 0
     assert bm.num_free_blocks == nb
     lib().pkv_sched_destroy(h)
+
+
+def test_request_tokens_negative_capacity_copies_nothing(native_lib):
+    from paged_kv_cache_138_gb300._lib import lib
+    from paged_kv_cache_138_gb300.block_manager import BlockManager
+    bm = BlockManager(8, 16, True)
+    h = lib().pkv_sched_create(bm._h, 2, 4, 16, 0, 0, ctypes.c_uint64(1), 100)
+    try:
+        p = np.array([5, 6, 7], np.int32)
+        assert lib().pkv_sched_add_request(h, 3, p.ctypes.data_as(ctypes.c_void_p), 3, 2) == 0
+        out = np.full(4, -7, np.int32)
+        q = out.ctypes.data_as(ctypes.c_void_p)
+        assert lib().pkv_sched_request_tokens(h, 3, q, -1) == 3
+        assert (out == -7).all()
+        assert lib().pkv_sched_request_tokens(h, 3, q, 2) == 3
+        assert list(out) == [5, 6, -7, -7]
+    finally:
+        lib().pkv_sched_destroy(h)
